@@ -1,0 +1,220 @@
+/*
+ * oq4.c -- CPU oracle (test infrastructure only; see oq4.h).
+ *
+ * Follows the page "Weight quantization", sections "How it works" and "Code".
+ * Build with contraction off so every f32 expression rounds exactly where the
+ * page's f32 code rounds:   gcc -O2 -std=c99 -ffp-contract=off -fPIC -shared
+ *
+ * OQ4_MUTANT (compile-time, default 0) plants one known mistake so that the
+ * test suite can show its pins catch it.  It is never set in a normal build.
+ */
+#include "oq4.h"
+
+#include <float.h>
+#include <math.h>
+#include <stddef.h>
+#include <string.h>
+
+#ifndef OQ4_MUTANT
+#define OQ4_MUTANT 0
+#endif
+
+int oq4_mutant(void) { return OQ4_MUTANT; }
+
+/* Rust's f32::clamp(lo, hi): below lo -> lo, above hi -> hi, else unchanged. */
+static float clampf(float v, float lo, float hi)
+{
+    if (v < lo) return lo;
+    if (v > hi) return hi;
+    return v;
+}
+
+/* "round" on the page is Rust's f32::round: ties go away from zero, which is
+ * C99 roundf.  (Mutants 1/2 swap in ties-to-even, the torch/Python rule.) */
+static float round_code(float v)
+{
+#if OQ4_MUTANT == 1
+    return rintf(v);
+#else
+    return roundf(v);
+#endif
+}
+
+static float round_zero(float v)
+{
+#if OQ4_MUTANT == 2
+    return rintf(v);
+#else
+    return roundf(v);
+#endif
+}
+
+/* Where code `v` of flat weight index `idx` goes: byte idx/2, low nibble for
+ * an even index ("low nibble = even index" in the page's quantize). */
+static void put_code(uint8_t *packed, int64_t idx, uint8_t v)
+{
+#if OQ4_MUTANT == 3
+    packed[idx / 2] |= (uint8_t)(v << ((1 - (idx & 1)) * 4));
+#else
+    packed[idx / 2] |= (uint8_t)(v << ((idx & 1) * 4));
+#endif
+}
+
+static uint8_t get_code(const uint8_t *packed, int64_t idx)
+{
+    /* the inverse of put_code for the real layout */
+    uint8_t b = packed[idx / 2];
+    return (idx & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 0x0F);
+}
+
+int oq4_quantize_g(const float *w, int64_t N, int64_t K, int64_t G,
+                   uint8_t *packed, float *scale, uint8_t *zero)
+{
+    if (G <= 0 || K % G != 0 || ((N * K) & 1)) return -1;
+    memset(packed, 0, (size_t)(N * K / 2));
+
+    /* The page walks the flat weight vector in chunks of G; with K % G == 0 a
+     * chunk never straddles two rows, so chunk gi = n*(K/G) + g. */
+    const int64_t ngroups = N * K / G;
+    for (int64_t gi = 0; gi < ngroups; ++gi) {
+        const float *grp = w + gi * G;
+
+        /* 1. group minimum and maximum, folded from (f32::MAX, f32::MIN) */
+        float lo = FLT_MAX, hi = -FLT_MAX;
+        for (int64_t j = 0; j < G; ++j) {
+            lo = fminf(lo, grp[j]);
+            hi = fmaxf(hi, grp[j]);
+        }
+        /* 2. widen the range to contain 0 so that 0 is exactly representable */
+#if OQ4_MUTANT != 4
+        lo = fminf(lo, 0.0f);
+        hi = fmaxf(hi, 0.0f);
+#endif
+        /* 3. scale = (max - min) / (2^b - 1), or 1 when the range is empty */
+#if OQ4_MUTANT == 5
+        float s = (hi > lo) ? (hi - lo) / 16.0f : 1.0f;
+#else
+        float s = (hi > lo) ? (hi - lo) / 15.0f : 1.0f;
+#endif
+        /* 4. zero = round(-min / scale), clamped to [0, 15] */
+#if OQ4_MUTANT == 7
+        float z = clampf(round_zero(lo / s), 0.0f, 15.0f);
+#else
+        float z = clampf(round_zero(-lo / s), 0.0f, 15.0f);
+#endif
+        scale[gi] = s;
+        zero[gi] = (uint8_t)z;
+
+        /* 5. q = clamp(round(w / scale) + zero, 0, 15), then pack */
+        for (int64_t j = 0; j < G; ++j) {
+#if OQ4_MUTANT == 6
+            float qf = clampf(round_code(grp[j] / s + z), 0.0f, 15.0f);
+#else
+            float qf = clampf(round_code(grp[j] / s) + z, 0.0f, 15.0f);
+#endif
+            put_code(packed, gi * G + j, (uint8_t)qf);
+        }
+    }
+    return 0;
+}
+
+int oq4_quantize(const float *w, int64_t N, int64_t K,
+                 uint8_t *packed, float *scale, uint8_t *zero)
+{
+    return oq4_quantize_g(w, N, K, OQ4_G, packed, scale, zero);
+}
+
+/* w_hat = (q - zero) * scale  ("How it works", last formula).  Both factors
+ * are exact in double, and so is their product (4-bit x 24-bit). */
+static double what_at(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                      int64_t K, int64_t G, int64_t n, int64_t k)
+{
+    int64_t gi = n * (K / G) + k / G;
+#if OQ4_MUTANT == 11
+    gi = n * (K / G) + ((k + G / 2) / G) % (K / G);
+#endif
+    double q = (double)get_code(packed, n * K + k);
+    double z = (double)zero[gi];
+#if OQ4_MUTANT == 9
+    return (q + z) * (double)scale[gi];
+#else
+    return (q - z) * (double)scale[gi];
+#endif
+}
+
+void oq4_dequant_g(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                   int64_t N, int64_t K, int64_t G, double *w_hat)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w_hat[n * K + k] = what_at(packed, scale, zero, K, G, n, k);
+}
+
+void oq4_dot_naive(const float *x, int64_t M,
+                   const uint8_t *packed, const float *scale, const uint8_t *zero,
+                   int64_t N, int64_t K, int64_t n0, int64_t n1,
+                   double *y, double *absdot)
+{
+    const int64_t R = n1 - n0;
+    (void)N;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = n0; n < n1; ++n) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+#if OQ4_MUTANT == 10
+                /* transposed operand: reads w_hat[k][n] (square matrices) */
+                double wh = what_at(packed, scale, zero, K, OQ4_G, k % N, n % K);
+#else
+                double wh = what_at(packed, scale, zero, K, OQ4_G, n, k);
+#endif
+                double p = wh * (double)x[m * K + k];
+                acc += p;
+                aacc += fabs(p);
+            }
+            y[m * R + (n - n0)] = acc;
+            if (absdot) absdot[m * R + (n - n0)] = aacc;
+        }
+    }
+}
+
+void oq4_dot_factored(const float *x, int64_t M,
+                      const uint8_t *packed, const float *scale, const uint8_t *zero,
+                      int64_t N, int64_t K, int64_t n0, int64_t n1, float *y)
+{
+    const int64_t R = n1 - n0, NG = K / OQ4_G;
+    (void)N;
+    for (int64_t m = 0; m < M; ++m) {
+        const float *xr = x + m * K;
+        for (int64_t n = n0; n < n1; ++n) {
+            float acc = 0.0f;
+            for (int64_t g = 0; g < NG; ++g) {
+                const int64_t gi = n * NG + g;
+                const uint8_t *bytes = packed + (n * K + g * OQ4_G) / 2;
+                const float *xg = xr + g * OQ4_G;
+                float qx = 0.0f, sx = 0.0f;
+                for (int64_t b = 0; b < OQ4_G / 2; ++b) {
+                    float x0 = xg[2 * b], x1 = xg[2 * b + 1];
+                    qx += (float)(bytes[b] & 0x0F) * x0 + (float)(bytes[b] >> 4) * x1;
+                    sx += x0 + x1;
+                }
+#if OQ4_MUTANT == 8
+                acc += scale[gi] * qx;
+#else
+                acc += scale[gi] * (qx - (float)zero[gi] * sx);
+#endif
+            }
+            y[m * R + (n - n0)] = acc;
+        }
+    }
+}
+
+void oq4_xsum(const float *x, int64_t M, int64_t K, double *xsum)
+{
+    const int64_t NG = K / OQ4_G;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t g = 0; g < NG; ++g) {
+            double s = 0.0;
+            for (int64_t j = 0; j < OQ4_G; ++j) s += (double)x[m * K + g * OQ4_G + j];
+            xsum[m * NG + g] = s;
+        }
+}

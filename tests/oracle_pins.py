@@ -1,0 +1,280 @@
+"""Pins: checks that tie the CPU oracle to what the page and the mathematics
+fix, independently of the oracle's own code.  Each pin takes an ``Oracle``
+and raises AssertionError when the oracle violates it.  The same pins are run
+against deliberately broken builds of the oracle to show each planted mistake
+is caught (see test_oracle_mutants.py).
+
+Page cited throughout: "Weight quantization" (tirogla.com), sections
+"How it works" (formulas) and "Code" (quantize, dot, main).
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def read_golden(name: str) -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = (s.strip() for s in line.split("=", 1))
+            out[k] = int(v, 0) if v.startswith("0x") else float(v) if "." in v else int(v)
+    return out
+
+
+def _codes(packed: np.ndarray, n_total: int) -> np.ndarray:
+    """Unpack with the page's rule: byte idx/2, low nibble = even idx."""
+    flat = packed.reshape(-1)
+    c = np.empty(n_total, np.int64)
+    c[0::2] = flat & 0x0F
+    c[1::2] = flat >> 4
+    return c
+
+
+# ----------------------------------------------------------------------------- pins
+def pin_page_program(o):
+    """The page's own experiment (section "Code", main): the assert holds and
+    bits/weight, computed from the page's formula on the oracle's output
+    sizes, equals the golden value."""
+    gold = read_golden("page_program.txt")
+    n = gold["n"]
+    r, _ = synth.xorshift_stream(2 * n, gold["seed"])
+    w = (np.float32(gold["w_scale"]) * r[:n]).astype(np.float32)
+    x = r[n:]
+    packed, scale, zero = o.quantize(w)
+    dot = o.dot_factored(x, packed, scale, zero, 1, n)[0, 0]
+    # exact and scale accumulate in f32 in the page's order
+    exact = np.float32(0.0)
+    mag = np.float32(0.0)
+    for a, b in zip(w, x):
+        p = np.float32(a * b)
+        exact = np.float32(exact + p)
+        mag = np.float32(mag + np.float32(abs(p)))
+    assert abs(np.float32(dot - exact)) < np.float32(gold["bound_factor"]) * mag
+    bits = (packed.size * 8 + scale.size * 16 + zero.size * 4) / n
+    assert bits == gold["bits_per_weight"]
+    assert f"{bits:.3f}" == f"{gold['bits_per_weight_printed']:.3f}"
+
+
+def _integer_group():
+    """lo = -5, hi = 10 so that scale = 15/15 = 1 exactly and zero = 5; every
+    integer in [-5, 10] then has code w + 5 (closed form)."""
+    rng = np.random.default_rng(7)
+    v = rng.integers(-5, 11, size=128).astype(np.float32)
+    v[0], v[1] = -5.0, 10.0
+    return v
+
+
+def pin_closed_form_integer_group(o):
+    """Formulas of "How it works" on a group whose grid is the integers:
+    scale 1, zero 5, q = w + 5, w_hat = w exactly, and the byte layout of
+    quantize ("low nibble = even index")."""
+    v = _integer_group()
+    packed, scale, zero = o.quantize(v)
+    assert scale[0, 0] == np.float32(1.0)
+    assert zero[0, 0] == 5
+    q = (v + 5).astype(np.int64)
+    expect_bytes = (q[0::2] | (q[1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(packed.reshape(-1), expect_bytes)
+    wh = o.dequant(packed, scale, zero, 1, 128)
+    assert np.array_equal(wh.reshape(-1), v.astype(np.float64))
+
+
+def pin_round_half_away_codes(o):
+    """Ties in w/scale round away from zero (the page's f32::round), and the
+    zero is added after rounding: with scale 1 and zero 5, w = 2.5 -> 3+5 = 8
+    and w = -2.5 -> -3+5 = 2 (ties-to-even would give 7 and 3; rounding
+    w/scale + zero would give 8 and 3)."""
+    v = _integer_group()
+    v[2], v[3] = 2.5, -2.5
+    packed, scale, zero = o.quantize(v)
+    assert scale[0, 0] == 1.0 and zero[0, 0] == 5
+    c = _codes(packed, 128)
+    assert c[2] == 8 and c[3] == 2
+
+
+def pin_round_half_away_zero(o):
+    """lo = -2.5, hi = 12.5: scale = 1 and -lo/scale = 2.5, a tie, so
+    zero = round(2.5) = 3 away from zero (2 under ties-to-even)."""
+    v = np.zeros(128, np.float32)
+    v[:64] = np.linspace(-2.0, 12.0, 64).round()
+    v[100], v[101] = -2.5, 12.5
+    packed, scale, zero = o.quantize(v)
+    assert scale[0, 0] == 1.0
+    assert zero[0, 0] == 3
+
+
+def pin_special_groups(o):
+    """Closed forms of the formulas on special groups:
+    all-zero -> scale 1 (the page's empty-range branch), zero 0, codes 0;
+    all-positive -> zero 0, the maximum maps to 15, 0 would map to 0;
+    all-negative -> zero 15, the minimum maps to 0;
+    constant c > 0 -> all codes 15; constant c < 0 -> all codes 0."""
+    rng = np.random.default_rng(11)
+    pos = rng.uniform(0.25, 2.0, 128).astype(np.float32)
+    neg = -rng.uniform(0.25, 2.0, 128).astype(np.float32)
+    w = np.stack([np.zeros(128, np.float32), pos, neg,
+                  np.full(128, 0.7, np.float32), np.full(128, -0.3, np.float32)])
+    packed, scale, zero = o.quantize(w)
+    c = _codes(packed, w.size).reshape(5, 128)
+    assert scale[0, 0] == 1.0 and zero[0, 0] == 0 and not c[0].any()
+    assert zero[1, 0] == 0 and c[1][np.argmax(pos)] == 15
+    # all-positive: lo clamps to 0, so 15*scale reproduces the maximum to f32 rounding
+    assert abs(15.0 * float(scale[1, 0]) - float(pos.max())) <= 2 ** -20 * float(pos.max())
+    assert zero[2, 0] == 15 and c[2][np.argmin(neg)] == 0
+    assert abs(15.0 * float(scale[2, 0]) + float(neg.min())) <= 2 ** -20 * float(-neg.min())
+    assert (c[3] == 15).all() and zero[3, 0] == 0
+    assert (c[4] == 0).all() and zero[4, 0] == 15
+
+
+def _random_groups(rng, N=48, K=512):
+    """Groups of varied character: symmetric, skewed, one-signed, with a huge
+    outlier, tiny magnitudes, and exact zeros sprinkled in."""
+    W = rng.normal(0.0, 0.02, (N, K)).astype(np.float32)
+    W[0:4] = np.abs(W[0:4])                       # all >= 0
+    W[4:8] = -np.abs(W[4:8])                      # all <= 0
+    W[8:12] *= np.float32(1e-30)                  # tiny
+    W[12:16, ::37] *= np.float32(100.0)           # outliers
+    W[16:20] += np.float32(0.05)                  # skewed
+    W[rng.random((N, K)) < 0.03] = 0.0            # exact zeros
+    return W
+
+
+def pin_zero_exact(o):
+    """The range is widened to contain 0 ("keep 0 exactly representable"),
+    so every w == 0 reconstructs to exactly 0, and 0 <= zero <= 15."""
+    rng = np.random.default_rng(3)
+    W = _random_groups(rng)
+    N, K = W.shape
+    packed, scale, zero = o.quantize(W)
+    wh = o.dequant(packed, scale, zero, N, K)
+    assert (zero <= 15).all()
+    assert (wh[W == 0] == 0.0).all()
+
+
+def pin_half_step(o):
+    """Rounding error is at most half a step: |w - w_hat| <= scale/2 for every
+    element, the clamped extremes included (lo >= -zero*s - s/2 since zero
+    rounds -lo/s; hi <= (15-zero)*s + s/2 since hi - lo = 15 s).  Checked in
+    double with a few f32 ulps of slack for the rounding of s itself."""
+    rng = np.random.default_rng(5)
+    W = _random_groups(rng)
+    N, K = W.shape
+    packed, scale, zero = o.quantize(W)
+    wh = o.dequant(packed, scale, zero, N, K)
+    s = np.repeat(scale.astype(np.float64), 128, axis=1)
+    err = np.abs(W.astype(np.float64) - wh)
+    assert (err <= 0.5 * s * (1 + 2 ** -16) + 16 * np.abs(W) * 2.0 ** -24).all()
+
+
+def pin_brute_force_tiny(o):
+    """Brute force over every group of size 2 and 3 on a grid of values
+    (multiples of 1/8 in [-1, 1]): the chosen code is a nearest point of the
+    group's 16-point grid (q - zero)*scale, up to the f32 rounding of w/scale,
+    scale spans the widened range (15*scale == hi - lo to f32 rounding) and
+    zero is the nearest integer to -lo/scale."""
+    vals = np.arange(-8, 9, dtype=np.float32) / np.float32(8.0)
+    for G in (2, 3):
+        groups = np.array(list(itertools.product(vals, repeat=G)), np.float32)
+        if G == 3:
+            groups = groups[::5]
+        W = groups.reshape(1, -1)
+        if W.shape[1] % 2:
+            W = W[:, :-G]
+        ng = W.shape[1] // G
+        packed, scale, zero = o.quantize(W, group=G)
+        c = _codes(packed, W.shape[1]).reshape(ng, G)
+        Wg = W.reshape(ng, G).astype(np.float64)
+        s = scale.reshape(ng).astype(np.float64)
+        z = zero.reshape(ng).astype(np.float64)
+        lo = np.minimum(Wg.min(1), 0.0)
+        hi = np.maximum(Wg.max(1), 0.0)
+        empty = hi == lo
+        assert (s[empty] == 1.0).all()
+        ne = ~empty
+        assert np.allclose(15.0 * s[ne], (hi - lo)[ne], rtol=2 ** -22, atol=0)
+        assert (np.abs(z[ne] - (-lo[ne] / s[ne])) <= 0.5 + 1e-6).all()
+        grid = (np.arange(16)[None, None, :] - z[:, None, None]) * s[:, None, None]
+        dist = np.abs(Wg[:, :, None] - grid)
+        chosen = np.take_along_axis(dist, c[:, :, None], axis=2)[:, :, 0]
+        # a near-tie may go either way because w/scale is an f32 quotient
+        slack = 2.0 ** -20 * s[:, None] + 2.0 ** -22 * np.abs(Wg)
+        assert (chosen <= dist.min(axis=2) + slack).all()
+
+
+def pin_dot_definition(o):
+    """The plain product against numpy's matmul of the dequantized matrix
+    (a library routine standing in for the definition sum_k w_hat*x), on a
+    non-square shape so that a transposed operand cannot pass."""
+    rng = np.random.default_rng(9)
+    for (N, K, M) in ((40, 384, 3), (256, 256, 2)):
+        W = rng.normal(0, 0.02, (N, K)).astype(np.float32)
+        X = rng.normal(0, 1, (M, K)).astype(np.float32)
+        packed, scale, zero = o.quantize(W)
+        wh = o.dequant(packed, scale, zero, N, K)
+        y, a = o.dot_naive(X, packed, scale, zero, N, K)
+        ref = X.astype(np.float64) @ wh.T
+        aref = np.abs(X.astype(np.float64)) @ np.abs(wh).T
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+        assert np.allclose(a, aref, rtol=1e-12, atol=1e-12)
+        # sub-range of rows gives the same numbers
+        y2, _ = o.dot_naive(X, packed, scale, zero, N, K, 5, 17)
+        assert np.array_equal(y2, y[:, 5:17])
+
+
+def pin_factored_identity(o):
+    """The factored group dot scale*(sum q*x - zero*sum x) ("How it works")
+    equals the naive dequantize-then-dot, up to f32 accumulation error."""
+    rng = np.random.default_rng(13)
+    N, K, M = 64, 1024, 3
+    W = _random_groups(rng, N, K)
+    X = rng.normal(0, 1, (M, K)).astype(np.float32)
+    packed, scale, zero = o.quantize(W)
+    yf = o.dot_factored(X, packed, scale, zero, N, K).astype(np.float64)
+    yn, a = o.dot_naive(X, packed, scale, zero, N, K)
+    assert (np.abs(yf - yn) <= 1e-5 * a + 1e-30).all()
+
+
+def pin_xsum(o):
+    """Activation group sums against numpy's sum."""
+    rng = np.random.default_rng(17)
+    X = rng.normal(0, 1, (3, 640)).astype(np.float32)
+    ref = X.astype(np.float64).reshape(3, 5, 128).sum(-1)
+    assert np.allclose(o.xsum(X), ref, rtol=1e-13, atol=1e-13)
+
+
+def pin_matrix_bound(o, N: int = 1024, K: int = 4096):
+    """The page's bound |err| < 0.02*sum|w*x| holds for every row of the
+    xorshift-drawn matrix (w = 0.02*U(-1,1) row-major, then x = U(-1,1)),
+    with the exact product taken on the unquantized weights in double."""
+    W, x = synth.xorshift_matrix(N, K)
+    packed, scale, zero = o.quantize(W)
+    y, _ = o.dot_naive(x, packed, scale, zero, N, K, threads=4)
+    exact = W.astype(np.float64) @ x.astype(np.float64)
+    mag = np.abs(W.astype(np.float64)) @ np.abs(x.astype(np.float64))
+    assert (np.abs(y[0] - exact) < 0.02 * mag).all()
+
+
+ALL_PINS = [
+    pin_page_program,
+    pin_closed_form_integer_group,
+    pin_round_half_away_codes,
+    pin_round_half_away_zero,
+    pin_special_groups,
+    pin_zero_exact,
+    pin_half_step,
+    pin_brute_force_tiny,
+    pin_dot_definition,
+    pin_factored_identity,
+    pin_xsum,
+    pin_matrix_bound,
+]
