@@ -1,0 +1,192 @@
+/*
+ * q4.h -- C ABI of the GB300 (sm_103a) weight-only INT4 group-128 library.
+ *
+ * What is computed (page "Weight quantization", tirogla.com, section "How it
+ * works" and section "Code"):
+ *   for each group of G = 128 consecutive weights of a row, along the input
+ *   dimension K:
+ *     lo = min(min w, 0), hi = max(max w, 0)
+ *     scale = (hi - lo) / 15            (1 when hi == lo)
+ *     zero  = clamp(round(-lo / scale), 0, 15)
+ *     q     = clamp(round(w / scale) + zero, 0, 15)
+ *     w_hat = (q - zero) * scale
+ *   and the product y[m][n] = sum_k w_hat[n][k] * x[m][k], evaluated per group
+ *   as scale * (sum q*x - zero * sum x) without materialising w_hat in HBM.
+ *   "round" rounds halfway cases away from zero; every division is an IEEE f32
+ *   division.
+ *
+ * Shapes and layouts (all row-major):
+ *   W       f32 [N][K]           K % 128 == 0, N >= 1
+ *   packed  u8  [N][K/2]         canonical layout: two codes per byte, the
+ *                                even k in the low nibble (page, "Code")
+ *   scale   f32 [N][K/128]       canonical
+ *   zero    u8  [N][K/128]       canonical
+ *   qw      opaque device buffer of q4_weight_bytes(N, K) bytes holding the
+ *           same codes, scales and zeros in the kernels' tiled layout
+ *           (written by q4_repack, read back by q4_unpack)
+ *   x       [M][K] of dtype xt,  y  [M][N] of dtype yt
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are device pointers unless stated; the caller owns all
+ *     memory.  No entry point allocates, frees or synchronises (except
+ *     q4_check), and every one is asynchronous on `stream` (NULL = the legacy
+ *     default stream).
+ *   - Argument errors are detected on the host before anything is launched,
+ *     and nothing is written: Q4_ERR_INVALID_ARG (bad sizes, NULL pointers,
+ *     K % 128 != 0, short workspace), Q4_ERR_UNSUPPORTED (M or dtype outside
+ *     what the entry point handles), Q4_ERR_MISALIGNED (a pointer without the
+ *     alignment stated for it).
+ *   - A failed launch returns Q4_ERR_CUDA (the CUDA error text is kept for
+ *     q4_last_cuda_error).  There is no fallback path of any kind.
+ *   - Weights must be finite; NaN or infinite weights give unspecified codes.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *q4_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_INVALID_ARG = 1,
+    Q4_ERR_UNSUPPORTED = 2,
+    Q4_ERR_MISALIGNED = 3,
+    Q4_ERR_CUDA = 4,
+    Q4_ERR_TIMEOUT = 5
+} q4_status;
+
+typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
+
+#define Q4_GROUP 128
+#define Q4_TILE_ROWS 16
+#define Q4_TILE_BYTES 1104 /* 16 rows x 128 k: 1024 B codes + 64 B scales + 16 B zeros */
+#define Q4_GEMV_MAX_M 16
+
+/*
+ * Round-to-nearest quantization and nibble packing of a row-major f32 matrix
+ * (page "Weight quantization": "How it works" formulas, function `quantize`).
+ * w: [N][K] f32, 16-byte aligned.  Writes packed [N][K/2], scale [N][K/128],
+ * zero [N][K/128] (canonical layout).  Bit-identical to the page's f32
+ * arithmetic: IEEE division, ties away from zero, no contraction.
+ * Errors: INVALID_ARG for N < 1, K < 128, K % 128 != 0 or a NULL pointer;
+ * MISALIGNED unless w is 16-byte aligned.
+ */
+q4_status q4_quantize(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                      uint8_t *zero, q4_stream_t stream);
+
+/* Bytes of the tiled kernel layout for an N x K matrix: ceil(N/16) row tiles
+ * times K/128 groups times Q4_TILE_BYTES.  0 for invalid sizes. */
+size_t q4_weight_bytes(int64_t N, int64_t K);
+
+/*
+ * Canonical -> tiled kernel layout ("packed formats with scale interleaving",
+ * page "quant_llm_arch_2k", section "Memory Layout"; the offline pre-shuffle
+ * of page "Weight quantization", section "Code", closing remark).  A
+ * bijection: q4_unpack inverts it exactly.  Rows N..16*ceil(N/16)-1 of the
+ * last tile are written as zeros.  qw must be 16-byte aligned and hold
+ * q4_weight_bytes(N, K) bytes; it may not overlap the inputs.
+ * Tile (row tile rt, group g) starts at byte (rt*(K/128) + g) * 1104:
+ *   bytes [0, 1024): 32 lanes x 2 chunks of 16 B; chunk c of lane l = 4 words,
+ *     word i covers k-step j = 4c+i (k = 128g + 16j .. +15) for tile rows
+ *     r = l/4 and r+8 and k offsets 2(l%4) + {0,1,8,9}; nibble fields (bit
+ *     offset: row, k offset) 0:(r,0) 16:(r,1) 4:(r+8,0) 20:(r+8,1)
+ *     8:(r+8,8) 24:(r+8,9) 12:(r,8) 28:(r,9)
+ *   bytes [1024, 1088): f32 scale pairs (s[i], s[i+8]) for i = 0..7
+ *   bytes [1088, 1104): u8 zero pairs (z[i], z[i+8]) for i = 0..7
+ */
+q4_status q4_repack(const uint8_t *packed, const float *scale, const uint8_t *zero, int64_t N,
+                    int64_t K, void *qw, q4_stream_t stream);
+
+/* Tiled kernel layout -> canonical layout (exact inverse of q4_repack). */
+q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                    uint8_t *zero, q4_stream_t stream);
+
+/*
+ * Activation group sums, xsum[m][g] = sum_{k in group g} x[m][k] accumulated
+ * in f32 (the "sum x" of the factored group dot, page "Weight quantization",
+ * "How it works").  x: [M][K] of dtype xt; xsum: f32 [M][K/128].
+ */
+q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
+                  q4_stream_t stream);
+
+/* Workspace bytes q4_gemv needs for this problem on the current device (0
+ * when no split over K is used).  Layout: split-K arrival counters (one u32
+ * per 64 output rows, padded to 256 B) followed by f32 partial sums.  The
+ * counter block must be zero before the first call (zero-fill the buffer
+ * once after allocation); every completed call leaves it zero again.  Calls
+ * that may run concurrently need separate workspaces. */
+size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Decode GEMV, 1 <= M <= 16:  y[m][n] = sum over groups g of
+ *   scale[n][g] * (sum_{k in g} q[n][k] * x[m][k] - zero[n][g] * sum_{k in g} x[m][k])
+ * (page "Weight quantization", "How it works", factored group dot; function
+ * `dot`), fp32 accumulation, dequantization fused in registers.
+ * x: [M][K] (xt = F32, BF16 or F16), qw: tiled layout from q4_repack, y:
+ * [M][N] (yt = F32, BF16 or F16, rounded to nearest even from f32).
+ * x, qw, y and workspace must be 16-byte aligned; workspace may be NULL when
+ * q4_gemv_workspace_bytes returns 0.  Errors: UNSUPPORTED for M outside
+ * [1, 16]; INVALID_ARG for bad sizes or a short workspace.
+ */
+q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                  void *y, q4_dtype yt, void *workspace, size_t workspace_bytes,
+                  q4_stream_t stream);
+
+/* Kernel choice for q4_gemv_path: AUTO is what q4_gemv uses (FMA for M = 1,
+ * MMA otherwise).  FMA: CUDA-core f32 FMAs on codes turned into f32 in
+ * registers (M = 1 only).  MMA: m16n8k16 tensor-core MMAs with the codes as
+ * bf16/f16 A fragments built in registers and the batch as the n dimension. */
+#define Q4_PATH_AUTO 0
+#define Q4_PATH_FMA 1
+#define Q4_PATH_MMA 2
+
+/* q4_gemv with an explicit kernel choice (same arguments, same results within
+ * the f32 accumulation tolerance).  UNSUPPORTED for FMA with M != 1. */
+q4_status q4_gemv_path(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                       const void *qw, void *y, q4_dtype yt, void *workspace,
+                       size_t workspace_bytes, int path, q4_stream_t stream);
+
+/* Diagnostic for the bounded-wait machinery: launches the q4_gemv kernel for
+ * this problem with its copy engine told to issue nothing, so every consumer
+ * wait runs out after 20 ms.  The kernel then writes no output and raises the
+ * device error word; a following q4_check(stream) returns Q4_ERR_TIMEOUT.
+ * No GPU fault is involved and the context stays usable. */
+q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                                   const void *qw, void *y, q4_dtype yt, void *workspace,
+                                   size_t workspace_bytes, q4_stream_t stream);
+
+/*
+ * Large-M W4A16 GEMM, Y[M][N] = X[M][K] * W_hat[N][K]^T (prefill; page
+ * "LLM Quantization Architecture in Depth", section "Kernels and memory
+ * layout": dequantize in shared memory and feed the tensor cores in the same
+ * pass).  W_hat is formed tile by tile in shared memory as bf16 (or f16 for
+ * f16 activations) and multiplied on the tcgen05 tensor cores with f32
+ * accumulators in tensor memory.  x: [M][K] BF16 or F16; y: [M][N] of yt.
+ * Requires M >= 1, N % 16 == 0; x, qw and y 16-byte aligned.
+ */
+q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                  void *y, q4_dtype yt, q4_stream_t stream);
+
+/* Synchronises `stream` and reports errors raised on the device since the
+ * last check: Q4_ERR_TIMEOUT when a bounded wait inside a kernel gave up
+ * (the kernel then returned without writing its outputs), Q4_ERR_CUDA for a
+ * CUDA error, else Q4_OK.  Clears the device error word. */
+q4_status q4_check(q4_stream_t stream);
+
+/* Static description of a status code. */
+const char *q4_status_str(q4_status status);
+
+/* Text of the most recent CUDA error seen by this library in this thread. */
+const char *q4_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4_H */

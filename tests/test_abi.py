@@ -1,0 +1,81 @@
+"""The C-ABI library: loads, exports every symbol include/q4.h declares, and
+rejects bad arguments on the host before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4.h")
+LIB = os.path.join(ROOT, "weight_only_int4_group_gb300", "libq4.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("q4_quantize", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemm",
+                 "q4_check", "q4_status_str", "q4_weight_bytes", "q4_gemv_workspace_bytes"):
+        assert must in names
+
+
+def test_header_is_plain_c():
+    text = open(HEADER).read()
+    assert "torch" not in text.lower().replace("pytorch", "")
+    assert "#include <cuda" not in text
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in q4.h but not exported"
+
+
+def test_status_strings(lib):
+    lib.q4_status_str.restype = ctypes.c_char_p
+    for s in range(6):
+        assert lib.q4_status_str(s)
+    assert b"unknown" in lib.q4_status_str(99)
+
+
+def test_weight_bytes(lib):
+    lib.q4_weight_bytes.restype = ctypes.c_size_t
+    lib.q4_weight_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.q4_weight_bytes(16, 128) == 1104
+    assert lib.q4_weight_bytes(17, 256) == 2 * 2 * 1104
+    assert lib.q4_weight_bytes(28672, 8192) == 1792 * 64 * 1104
+    assert lib.q4_weight_bytes(16, 100) == 0
+    assert lib.q4_weight_bytes(0, 128) == 0
+
+
+def test_host_side_argument_errors(lib):
+    P, I, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.q4_quantize.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_gemv.argtypes = [P, S, I, I, I, P, P, S, P, ctypes.c_size_t, P]
+    lib.q4_repack.argtypes = [P, P, P, I, I, P, P]
+    fake = 4096  # never dereferenced: every case below fails its host checks first
+    # NULL pointer, bad K, K not a multiple of 128
+    assert lib.q4_quantize(None, 4, 128, fake, fake, fake, None) == 1
+    assert lib.q4_quantize(fake, 4, 100, fake, fake, fake, None) == 1
+    assert lib.q4_quantize(fake, 0, 128, fake, fake, fake, None) == 1
+    # misaligned input
+    assert lib.q4_quantize(fake + 4, 4, 128, fake, fake, fake, None) == 3
+    assert lib.q4_repack(fake, fake, fake, 4, 128, fake + 8, None) == 3
+    # GEMV: M outside [1, 16] is unsupported, bad dtype unsupported, misaligned
+    assert lib.q4_gemv(fake, 1, 0, 64, 128, fake, fake, 0, None, 0, None) == 2
+    assert lib.q4_gemv(fake, 1, 17, 64, 128, fake, fake, 0, None, 0, None) == 2
+    assert lib.q4_gemv(fake, 7, 1, 64, 128, fake, fake, 0, None, 0, None) == 2
+    assert lib.q4_gemv(fake + 2, 1, 1, 64, 128, fake, fake, 0, None, 0, None) == 3
+    assert lib.q4_gemv(fake, 1, 1, 64, 129, fake, fake, 0, None, 0, None) == 1

@@ -1,0 +1,124 @@
+"""GPU quantize/pack against the oracle: codes, scales and zeros bit-exact;
+repack/unpack round trip; activation group sums."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _edge_matrix(N, K, seed):
+    rng = np.random.default_rng(seed)
+    W = rng.normal(0, 0.02, (N, K)).astype(np.float32)
+    if N >= 12:
+        W[0] = 0.0                                       # all-zero groups (empty range)
+        W[1] = np.abs(W[1])                              # all >= 0
+        W[2] = -np.abs(W[2])                             # all <= 0
+        W[3] = np.float32(0.37)                          # constant > 0
+        W[4] = np.float32(-0.11)                         # constant < 0
+        W[5] = rng.integers(-5, 11, K).astype(np.float32)  # scale 1, zero 5, exact ties below
+        W[5, ::128] = -5.0
+        W[5, 1::128] = 10.0
+        W[5, 2::7] = 2.5                                 # ties of w/scale
+        W[5, 3::7] = -2.5
+        W[6] *= np.float32(1e-30)                        # subnormal-range scales
+        W[7, ::37] *= np.float32(100.0)                  # outliers
+        W[8] += np.float32(0.05)                         # skewed
+        W[9, ::128] = -2.5                               # zero tie: -lo/scale = 2.5
+        W[9, 1::128] = 12.5
+        W[9, 2::128] = 0.0
+        W[10][rng.random(K) < 0.2] = 0.0                 # exact zeros
+        W[11] = -0.0                                     # negative zeros
+    return W
+
+
+SHAPES = [(1, 128), (2, 256), (12, 128), (200, 1024), (33, 4096), (16, 11008)]
+
+
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_quantize_bit_exact(N, K):
+    W = _edge_matrix(N, K, seed=N * 7 + K)
+    import weight_only_int4_group_gb300 as q4
+    p, s, z = q4.quantize(dev_f32(W))
+    torch.cuda.synchronize()
+    po, so, zo = oracle.load().quantize(W)
+    assert np.array_equal(p.cpu().numpy(), po)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zo)
+
+
+def test_quantize_page_program():
+    import weight_only_int4_group_gb300 as q4
+    w, _ = synth.page_program()
+    p, s, z = q4.quantize(dev_f32(w.reshape(1, -1)))
+    po, so, zo = oracle.load().quantize(w)
+    assert np.array_equal(p.cpu().numpy(), po)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zo)
+
+
+def test_quantize_xorshift_4096_full():
+    """The whole 4096 x 4096 single-GEMV matrix (w = 0.02*U(-1,1), xorshift)."""
+    import weight_only_int4_group_gb300 as q4
+    W, _ = synth.xorshift_matrix(4096, 4096)
+    p, s, z = q4.quantize(dev_f32(W))
+    po, so, zo = oracle.load().quantize(W)
+    assert np.array_equal(p.cpu().numpy(), po)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zo)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (15, 256), (16, 128), (17, 384), (200, 1024)])
+def test_repack_unpack_round_trip(N, K):
+    import weight_only_int4_group_gb300 as q4
+    rng = np.random.default_rng(N + K)
+    packed = torch.from_numpy(rng.integers(0, 256, (N, K // 2), dtype=np.uint8)).cuda()
+    scale = torch.from_numpy(rng.normal(0, 1, (N, K // 128)).astype(np.float32)).cuda()
+    zero = torch.from_numpy(rng.integers(0, 16, (N, K // 128), dtype=np.uint8)).cuda()
+    qw = q4.repack(packed, scale, zero, N, K)
+    assert qw.numel() == q4.weight_bytes(N, K)
+    p2, s2, z2 = q4.unpack(qw, N, K)
+    assert torch.equal(p2, packed)
+    assert torch.equal(s2.view(torch.int32), scale.view(torch.int32))
+    assert torch.equal(z2, zero)
+    # padded rows of the last tile are zero
+    ntiles = (N + 15) // 16
+    if N % 16:
+        t = qw.view(ntiles, K // 128, 1104)[-1].cpu().numpy()
+        # scale pairs of rows >= N (within the tile) are 0.0
+        sp = t[:, 1024:1088].view(np.float32).reshape(K // 128, 8, 2)
+        for r in range(N % 16, 16):
+            assert (sp[:, r % 8, r // 8] == 0).all()
+
+
+def test_repack_field_layout():
+    """One code placed at a known (row, k) lands in the nibble field the
+    header documents."""
+    import weight_only_int4_group_gb300 as q4
+    N, K = 16, 128
+    for (row, k, lane, chunk, word, shift) in [
+            (0, 0, 0, 0, 0, 0), (0, 1, 0, 0, 0, 16), (8, 0, 0, 0, 0, 4), (8, 1, 0, 0, 0, 20),
+            (8, 8, 0, 0, 0, 8), (8, 9, 0, 0, 0, 24), (0, 8, 0, 0, 0, 12), (0, 9, 0, 0, 0, 28),
+            (3, 6, 15, 0, 0, 0), (3, 16 * 5 + 7, 15, 1, 1, 16), (11, 16 * 7 + 15, 15, 1, 3, 24)]:
+        packed = np.zeros((N, K // 2), np.uint8)
+        packed[row, k // 2] = (9 << 4) if k % 2 else 9
+        qw = q4.repack(torch.from_numpy(packed).cuda(), torch.zeros((N, 1), device="cuda"),
+                       torch.zeros((N, 1), dtype=torch.uint8, device="cuda"), N, K).cpu().numpy()
+        words = qw[:1024].view(np.uint32).reshape(2, 32, 4)
+        expect = np.zeros_like(words)
+        expect[chunk, lane, word] = 9 << shift
+        assert np.array_equal(words, expect), (row, k)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_xsum(dtype):
+    import weight_only_int4_group_gb300 as q4
+    from gpu_helpers import x_for
+    x, xf = x_for(dtype, 5, 1024, seed=3)
+    got = q4.xsum(x).cpu().numpy().astype(np.float64)
+    ref = oracle.load().xsum(xf)
+    assert np.allclose(got, ref, rtol=1e-5, atol=1e-4)

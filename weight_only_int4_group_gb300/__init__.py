@@ -1,0 +1,216 @@
+"""Python binding of libq4.so, the GB300 weight-only INT4 group-128 library.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch is used for device memory and the current CUDA stream.  Importing
+this package fails loudly when libq4.so has not been built; there is no
+fallback of any kind.
+
+Names follow include/q4.h: quantize, repack, unpack, xsum, gemv, gemm,
+check, weight_bytes, gemv_workspace_bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq4.so")
+GROUP = 128
+TILE_ROWS = 16
+TILE_BYTES = 1104
+GEMV_MAX_M = 16
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
+F32, BF16, F16 = 0, 1, 2
+PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
+
+_DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.q4_status_str(status).decode()
+        if status == ERR_CUDA:
+            msg += ": " + _lib.q4_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    lib.q4_quantize.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_weight_bytes.argtypes = [I, I]
+    lib.q4_weight_bytes.restype = Z
+    lib.q4_repack.argtypes = [P, P, P, I, I, P, P]
+    lib.q4_unpack.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_xsum.argtypes = [P, S, I, I, P, P]
+    lib.q4_gemv_workspace_bytes.argtypes = [I, I, I]
+    lib.q4_gemv_workspace_bytes.restype = Z
+    lib.q4_gemv.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
+    lib.q4_gemv_path.argtypes = [P, S, I, I, I, P, P, S, P, Z, S, P]
+    lib.q4_gemv_timeout_selftest.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
+    lib.q4_gemm.argtypes = [P, S, I, I, I, P, P, S, P]
+    lib.q4_check.argtypes = [P]
+    lib.q4_status_str.argtypes = [S]
+    lib.q4_status_str.restype = ctypes.c_char_p
+    lib.q4_last_cuda_error.restype = ctypes.c_char_p
+    for f in ("q4_quantize", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemv_path",
+              "q4_gemv_timeout_selftest", "q4_gemm", "q4_check"):
+        getattr(lib, f).restype = S
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ctypes library (for callers that marshal their own pointers)."""
+    return _lib
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ok(status: int, where: str):
+    if status != OK:
+        raise Q4Error(status, where)
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------ API
+def weight_bytes(N: int, K: int) -> int:
+    return int(_lib.q4_weight_bytes(N, K))
+
+
+def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.q4_gemv_workspace_bytes(M, N, K))
+
+
+def quantize(w: torch.Tensor, stream=None):
+    """w f32 [N][K] (cuda) -> (packed u8 [N][K/2], scale f32 [N][K/128], zero u8 [N][K/128])."""
+    _cuda(w, "w")
+    if w.dtype != torch.float32 or w.dim() != 2:
+        raise ValueError("w must be a 2-D float32 tensor")
+    N, K = w.shape
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    scale = torch.empty((N, max(K // GROUP, 1)), dtype=torch.float32, device=w.device)
+    zero = torch.empty((N, max(K // GROUP, 1)), dtype=torch.uint8, device=w.device)
+    _ok(_lib.q4_quantize(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(),
+                         zero.data_ptr(), _stream(stream)), "q4_quantize")
+    return packed, scale, zero
+
+
+def repack(packed: torch.Tensor, scale: torch.Tensor, zero: torch.Tensor, N: int, K: int,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Canonical arrays -> tiled kernel layout (uint8 [weight_bytes(N, K)])."""
+    for t, n in ((packed, "packed"), (scale, "scale"), (zero, "zero")):
+        _cuda(t, n)
+    nb = weight_bytes(N, K)
+    if nb == 0:
+        raise ValueError(f"invalid shape {N}x{K}")
+    if out is None:
+        out = torch.empty(nb, dtype=torch.uint8, device=packed.device)
+    _ok(_lib.q4_repack(packed.data_ptr(), scale.data_ptr(), zero.data_ptr(), N, K,
+                       out.data_ptr(), _stream(stream)), "q4_repack")
+    return out
+
+
+def unpack(qw: torch.Tensor, N: int, K: int, stream=None):
+    _cuda(qw, "qw")
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=qw.device)
+    scale = torch.empty((N, K // GROUP), dtype=torch.float32, device=qw.device)
+    zero = torch.empty((N, K // GROUP), dtype=torch.uint8, device=qw.device)
+    _ok(_lib.q4_unpack(qw.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(),
+                       zero.data_ptr(), _stream(stream)), "q4_unpack")
+    return packed, scale, zero
+
+
+def xsum(x: torch.Tensor, stream=None) -> torch.Tensor:
+    _cuda(x, "x")
+    M, K = x.shape
+    out = torch.empty((M, K // GROUP), dtype=torch.float32, device=x.device)
+    _ok(_lib.q4_xsum(x.data_ptr(), _DTYPE[x.dtype], M, K, out.data_ptr(), _stream(stream)),
+        "q4_xsum")
+    return out
+
+
+@dataclass
+class QWeight:
+    """A weight matrix in the tiled kernel layout."""
+    data: torch.Tensor  # uint8 [weight_bytes(N, K)]
+    N: int
+    K: int
+
+    @classmethod
+    def from_float(cls, w: torch.Tensor, stream=None) -> "QWeight":
+        N, K = w.shape
+        packed, scale, zero = quantize(w, stream)
+        return cls(repack(packed, scale, zero, N, K, stream=stream), N, K)
+
+
+def workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
+    """A zero-filled workspace for q4_gemv (None when none is needed)."""
+    nb = gemv_workspace_bytes(M, N, K)
+    if nb == 0:
+        return None
+    return torch.zeros(nb, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+def gemv(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
+         ws: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y [M][N] = x [M][K] * w_hat^T for 1 <= M <= 16."""
+    _cuda(x, "x")
+    M, K = x.shape
+    if K != qw.K:
+        raise ValueError(f"x has K={K}, weight has K={qw.K}")
+    if out is None:
+        out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)
+    if ws is None:
+        ws = workspace(M, qw.N, K, x.device)
+    wsp, wsb = (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
+    _ok(_lib.q4_gemv_path(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
+                          out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, path, _stream(stream)),
+        "q4_gemv")
+    return out
+
+
+def gemv_timeout_selftest(x: torch.Tensor, qw: QWeight, out: torch.Tensor,
+                          ws: torch.Tensor | None = None, stream=None) -> None:
+    M, K = x.shape
+    wsp, wsb = (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
+    _ok(_lib.q4_gemv_timeout_selftest(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K,
+                                      qw.data.data_ptr(), out.data_ptr(), _DTYPE[out.dtype],
+                                      wsp, wsb, _stream(stream)), "q4_gemv_timeout_selftest")
+
+
+def gemm(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Y [M][N] = X [M][K] * w_hat^T on the tcgen05 tensor cores (large M)."""
+    _cuda(x, "x")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)
+    _ok(_lib.q4_gemm(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
+                     out.data_ptr(), _DTYPE[out.dtype], _stream(stream)), "q4_gemm")
+    return out
+
+
+def check(stream=None) -> int:
+    """Synchronise and return the library status (raises nothing)."""
+    return int(_lib.q4_check(_stream(stream)))

@@ -1,0 +1,184 @@
+// common.cuh -- shared constants, inline-PTX helpers and internal launcher
+// declarations of the q4 library (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/q4.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "this library targets sm_103a (Blackwell) only"
+#endif
+
+namespace q4 {
+
+constexpr int G = Q4_GROUP;                 // weights per group along K
+constexpr int TILE_ROWS = Q4_TILE_ROWS;     // rows per tile
+constexpr int TILE_BYTES = Q4_TILE_BYTES;   // 1104
+constexpr int CODE_BYTES = 1024;            // 16 rows x 128 codes / 2
+constexpr int SCALE_OFF = 1024;             // 8 pairs of f32 scales
+constexpr int ZERO_OFF = 1088;              // 8 pairs of u8 zeros
+
+// Device error word (one per device, defined in api.cu, its address passed to
+// every kernel that waits): bit 0 = a bounded wait timed out.  Read and
+// cleared by q4_check.
+constexpr unsigned int ERR_TIMEOUT = 1u;
+unsigned int *device_error_word();  // host: address on the current device
+
+// ----------------------------------------------------------------- inline PTX
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (after raising the
+// device error word and the CTA's abort flag) when `limit_ns` elapses or when
+// another role of the CTA has already aborted.  Never spins without bound.
+// With honor_abort == false (used to drain copies already in flight before
+// a CTA exits) only the time bound ends the wait.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, uint64_t limit_ns,
+                                                  unsigned int *err, bool honor_abort = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honor_abort && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk asynchronous copy global -> shared (TMA engine, no tensor map),
+// completion counted in bytes on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// d = (a & b) | c  as one LOP3
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ------------------------------------------------------------ dtype helpers
+__device__ __forceinline__ float load_x_f32(const void *x, q4_dtype xt, int64_t i)
+{
+    if (xt == Q4_F32) return static_cast<const float *>(x)[i];
+    const uint16_t b = static_cast<const uint16_t *>(x)[i];
+    if (xt == Q4_BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    __half_raw hr;
+    hr.x = b;
+    return __half2float(__half(hr));
+}
+
+// ------------------------------------------------------- internal launchers
+struct GemvArgs {
+    const void *x;
+    q4_dtype xt;
+    int M, N, K;
+    const uint8_t *qw;
+    void *y;
+    q4_dtype yt;
+    float *partial;       // [KS][M][ntiles*16] when KS > 1
+    unsigned int *count;  // [nrb] split-K arrival counters when KS > 1
+    int ks, gs;           // number of K slices, groups per slice
+    uint64_t wait_ns;     // bound of every mbarrier wait
+    unsigned int *err;    // device error word
+    int debug_no_copy;    // producer issues no copy (exercises the timeout path)
+};
+
+enum GemvPath { PATH_AUTO = 0, PATH_FMA = 1, PATH_MMA = 2 };
+
+struct GemvPlan {
+    int path;
+    int rb;      // row tiles per CTA
+    int ks, gs;  // K slices, groups per slice
+    int nrb;     // row blocks
+    size_t workspace;
+};
+
+GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
+size_t counters_bytes(int nrb);  // split-K counter block at the start of the workspace
+cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
+
+cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                            uint8_t *zero, cudaStream_t s);
+cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                          int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
+cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                          uint8_t *zero, cudaStream_t s);
+cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
+                        cudaStream_t s);
+
+}  // namespace q4

@@ -1,0 +1,240 @@
+// quantize.cu -- GPU round-to-nearest quantize/pack, the canonical <-> tiled
+// layout conversion, and activation group sums.
+//
+// Quantize follows the page "Weight quantization" (tirogla.com), section
+// "How it works" (scale/zero/q formulas) and section "Code" (function
+// `quantize`): f32 throughout, IEEE division, ties away from zero, zero added
+// after rounding, low nibble = even index.  This file is compiled with
+// --fmad=false and every rounding step uses an explicit _rn intrinsic, so the
+// codes, scales and zeros are bit-identical to the page's f32 arithmetic.
+#include "common.cuh"
+
+namespace q4 {
+
+// One warp per group of 128 weights: each lane holds 4 consecutive weights
+// (one 16-byte load), min/max by butterfly shuffles (exact, order-free),
+// then every lane quantizes its 4 weights and stores 2 packed bytes.
+__global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, int64_t ngroups,
+                                                  uint8_t *__restrict__ packed,
+                                                  float *__restrict__ scale,
+                                                  uint8_t *__restrict__ zero)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t gi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         gi < ngroups; gi += nwarps) {
+        const float4 v = __ldcs(reinterpret_cast<const float4 *>(w + gi * G) + lane);
+        float lo = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
+        float hi = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        // keep 0 exactly representable
+        lo = fminf(lo, 0.0f);
+        hi = fmaxf(hi, 0.0f);
+        const float s = (hi > lo) ? __fdiv_rn(__fsub_rn(hi, lo), 15.0f) : 1.0f;
+        const float z = fminf(fmaxf(roundf(__fdiv_rn(-lo, s)), 0.0f), 15.0f);
+
+        uint32_t q[4];
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float c = fminf(fmaxf(__fadd_rn(roundf(__fdiv_rn(e[i], s)), z), 0.0f), 15.0f);
+            q[i] = static_cast<uint32_t>(c);
+        }
+        // flat index gi*128 + 4*lane + i: even index in the low nibble
+        const uint16_t two = static_cast<uint16_t>(q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12));
+        reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = two;
+        if (lane == 0) {
+            scale[gi] = s;
+            zero[gi] = static_cast<uint8_t>(z);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- tiled layout
+// Word i of chunk c of lane l in tile (rt, g) covers k-step j = 4c+i, tile
+// rows r = l/4 and r+8, and k offsets 16j + 2(l%4) + {0,1,8,9} inside group
+// g.  Its eight nibble fields are filled from four canonical bytes (each byte
+// holds an even/odd k pair):
+//   B0 = (row r,   k0)     -> fields 0 (low nibble) and 16 (high nibble)
+//   B1 = (row r+8, k0)     -> fields 4 and 20
+//   B2 = (row r+8, k0 + 8) -> fields 8 and 24
+//   B3 = (row r,   k0 + 8) -> fields 12 and 28
+// with k0 = 16j + 2(l%4).  The low nibbles land in bits 0..15 and the high
+// nibbles in bits 16..31, so one mask-and-or yields a pair of 16-bit values.
+__device__ __forceinline__ uint32_t interleave4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3)
+{
+    const uint32_t lo = (b0 & 15u) | ((b1 & 15u) << 4) | ((b2 & 15u) << 8) | ((b3 & 15u) << 12);
+    const uint32_t hi = (b0 >> 4) | ((b1 >> 4) << 4) | ((b2 >> 4) << 8) | ((b3 >> 4) << 12);
+    return lo | (hi << 16);
+}
+
+// 69 sixteen-byte units per tile: 64 code chunks, 4 scale units, 1 zero unit.
+__global__ void k_repack(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
+                         const uint8_t *__restrict__ zero, int N, int K, int64_t ntiles_total,
+                         uint8_t *__restrict__ qw)
+{
+    const int NG = K / G;
+    const int64_t units = ntiles_total * 69;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = u / 69;
+        const int unit = static_cast<int>(u % 69);
+        const int64_t rt = tile / NG;
+        const int g = static_cast<int>(tile % NG);
+        const int64_t row0 = rt * TILE_ROWS;
+        uint8_t *dst = qw + tile * TILE_BYTES;
+        if (unit < 64) {
+            const int c = unit >> 5, l = unit & 31;
+            const int r = l >> 2, t = l & 3;
+            uint32_t out[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * c + i;
+                const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;  // even k
+                auto byte_at = [&](int64_t row, int64_t k) -> uint32_t {
+                    return row < N ? packed[row * (K / 2) + k / 2] : 0u;
+                };
+                out[i] = interleave4(byte_at(row0 + r, kb), byte_at(row0 + r + 8, kb),
+                                     byte_at(row0 + r + 8, kb + 8), byte_at(row0 + r, kb + 8));
+            }
+            *reinterpret_cast<uint4 *>(dst + (c * 32 + l) * 16) =
+                make_uint4(out[0], out[1], out[2], out[3]);
+        } else if (unit < 68) {
+            float sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int pair = 2 * (unit - 64) + (e >> 1);  // pair index 0..7
+                const int64_t row = row0 + pair + ((e & 1) ? 8 : 0);
+                sv[e] = row < N ? scale[row * NG + g] : 0.0f;
+            }
+            *reinterpret_cast<float4 *>(dst + SCALE_OFF + (unit - 64) * 16) =
+                make_float4(sv[0], sv[1], sv[2], sv[3]);
+        } else {
+            uint32_t zw[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const int pair = b >> 1;
+                const int64_t row = row0 + pair + ((b & 1) ? 8 : 0);
+                const uint32_t zv = row < N ? zero[row * NG + g] : 0u;
+                zw[b >> 2] |= zv << ((b & 3) * 8);
+            }
+            *reinterpret_cast<uint4 *>(dst + ZERO_OFF) = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+        }
+    }
+}
+
+// Inverse: one thread per code word (4 canonical bytes), plus one per tile
+// row-pair for the metadata.
+__global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t ntiles_total,
+                         uint8_t *__restrict__ packed, float *__restrict__ scale,
+                         uint8_t *__restrict__ zero)
+{
+    const int NG = K / G;
+    const int64_t units = ntiles_total * (256 + 8);
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = u / 264;
+        const int unit = static_cast<int>(u % 264);
+        const int64_t rt = tile / NG;
+        const int g = static_cast<int>(tile % NG);
+        const int64_t row0 = rt * TILE_ROWS;
+        const uint8_t *src = qw + tile * TILE_BYTES;
+        if (unit < 256) {
+            const int c = unit >> 7, l = (unit >> 2) & 31, i = unit & 3;
+            const int r = l >> 2, t = l & 3, j = 4 * c + i;
+            const uint32_t w = reinterpret_cast<const uint32_t *>(src)[(c * 32 + l) * 4 + i];
+            const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;
+            auto put = [&](int64_t row, int64_t k, int f) {
+                if (row < N) {
+                    const uint32_t lo = (w >> (4 * f)) & 15u, hi = (w >> (16 + 4 * f)) & 15u;
+                    packed[row * (K / 2) + k / 2] = static_cast<uint8_t>(lo | (hi << 4));
+                }
+            };
+            put(row0 + r, kb, 0);
+            put(row0 + r + 8, kb, 1);
+            put(row0 + r + 8, kb + 8, 2);
+            put(row0 + r, kb + 8, 3);
+        } else {
+            const int pair = unit - 256;
+            const float *sp = reinterpret_cast<const float *>(src + SCALE_OFF) + 2 * pair;
+            const uint8_t *zp = src + ZERO_OFF + 2 * pair;
+            if (row0 + pair < N) {
+                scale[(row0 + pair) * NG + g] = sp[0];
+                zero[(row0 + pair) * NG + g] = zp[0];
+            }
+            if (row0 + pair + 8 < N) {
+                scale[(row0 + pair + 8) * NG + g] = sp[1];
+                zero[(row0 + pair + 8) * NG + g] = zp[1];
+            }
+        }
+    }
+}
+
+// Activation group sums: one warp per (m, g), f32 accumulation.
+__global__ void k_xsum(const void *__restrict__ x, q4_dtype xt, int64_t M, int64_t K,
+                       float *__restrict__ xsum)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t NG = K / G, total = M * NG;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         id < total; id += nwarps) {
+        const int64_t m = id / NG, g = id % NG;
+        const int64_t base = m * K + g * G + 4 * lane;
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s += load_x_f32(x, xt, base + i);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) xsum[id] = s;
+    }
+}
+
+static int grid_for(int64_t work, int threads)
+{
+    int64_t b = (work + threads - 1) / threads;
+    const int64_t cap = 152LL * 32;
+    if (b > cap) b = cap;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                            uint8_t *zero, cudaStream_t s)
+{
+    const int64_t ngroups = N * K / G;
+    k_quantize<<<grid_for(ngroups * 32, 256), 256, 0, s>>>(w, ngroups, packed, scale, zero);
+    return cudaGetLastError();
+}
+
+cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                          int64_t N, int64_t K, uint8_t *qw, cudaStream_t s)
+{
+    const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
+    k_repack<<<grid_for(ntiles * 69, 256), 256, 0, s>>>(packed, scale, zero, static_cast<int>(N),
+                                                        static_cast<int>(K), ntiles, qw);
+    return cudaGetLastError();
+}
+
+cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                          uint8_t *zero, cudaStream_t s)
+{
+    const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
+    k_unpack<<<grid_for(ntiles * 264, 256), 256, 0, s>>>(qw, static_cast<int>(N),
+                                                         static_cast<int>(K), ntiles, packed,
+                                                         scale, zero);
+    return cudaGetLastError();
+}
+
+cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
+                        cudaStream_t s)
+{
+    const int64_t total = M * (K / G);
+    k_xsum<<<grid_for(total * 32, 256), 256, 0, s>>>(x, xt, M, K, xsum);
+    return cudaGetLastError();
+}
+
+}  // namespace q4
