@@ -1,0 +1,585 @@
+#!/usr/bin/env python
+"""Benchmark: W4A16 decode GEMV throughput (achieved HBM GB/s and fraction of
+peak) on the 70B-shaped decode step.
+
+Workload (default): one decode step = 80 layers x {qkv 10240x8192,
+o 8192x8192, gate+up fused 57344x8192, down 8192x28672} GEMVs at M = 1,
+asymmetric INT4 group-128 weights (N(0, 0.02), drawn on the device, quantized
+and packed by the library), bf16 activations N(0,1), f32 accumulation, bf16
+outputs.  36.9 GB of packed weights stream from HBM per step, far larger
+than L2, so no flush is needed between steps.  The step is captured once as a
+CUDA graph of 320 library launches and replayed.
+
+Prints ONE JSON line (rank 0).  Other measurements ride along in "rows":
+per-M sweep on the 70B MLP shapes, the quantizer's HBM throughput, and the
+large-M GEMM when available.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--M 1] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SIGMA = 0.02
+LAYER_SHAPES = [("qkv", 10240, 8192), ("o", 8192, 8192), ("gate_up", 57344, 8192),
+                ("down", 8192, 28672)]
+METRIC = "W4A16 GEMV achieved HBM GB/s & fraction of peak at M=1..16; us/call"
+
+
+def algo_bytes(M: int, N: int, K: int, xb: int = 2, yb: int = 2) -> int:
+    """Bytes a GEMV must move at minimum: 4-bit codes, one f32 scale and one
+    u8 zero per 128 weights, the activations and the outputs."""
+    return N * K // 2 + 5 * (N * K // 128) + M * K * xb + M * N * yb
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def profile_traffic(name: str, source_files: list) -> float | None:
+    """Per-launch DRAM bytes from a committed ncu summary, or None when the
+    kernel source changed since the capture (or no capture exists)."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    if h.group(1) != sources_hash(source_files):
+        return None
+    return float(m.group(1))
+
+
+def sources_hash(files: list) -> str:
+    d = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            d.update(fh.read())
+    return d.hexdigest()[:16]
+
+
+GEMV_SOURCES = ["weight_only_int4_group_gb300/csrc/gemv.cu",
+                "weight_only_int4_group_gb300/csrc/common.cuh"]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                p = [s.strip() for s in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ workload
+class Decode70B:
+    def __init__(self, q4, torch, M: int, layers: int, seed: int = 1000):
+        import synth
+        self.q4, self.torch, self.M, self.L = q4, torch, M, layers
+        dev = torch.device("cuda")
+        self.qw = []  # [layer][matrix] -> QWeight
+        wmax = max(N * K for _, N, K in LAYER_SHAPES)
+        scratch = torch.empty(wmax, dtype=torch.float32, device=dev)
+        for l in range(layers):
+            mats = []
+            for i, (_, N, K) in enumerate(LAYER_SHAPES):
+                w = scratch[:N * K].view(N, K)
+                synth.dev_normal_f32(w.data_ptr(), N * K, seed + 4 * l + i, 0, SIGMA)
+                packed, scale, zero = q4.quantize(w)
+                mats.append(q4.QWeight(q4.repack(packed, scale, zero, N, K), N, K))
+                del packed, scale, zero
+            self.qw.append(mats)
+        del scratch
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        # activations and outputs, one contiguous buffer each (one copy per step e2e)
+        self.x_off, self.y_off = [], []
+        xo = yo = 0
+        for l in range(layers):
+            xr, yr = [], []
+            for _, N, K in LAYER_SHAPES:
+                xr.append(xo)
+                yr.append(yo)
+                xo += M * K
+                yo += M * N
+            self.x_off.append(xr)
+            self.y_off.append(yr)
+        self.x_elems, self.y_elems = xo, yo
+        self.x = torch.empty(xo, dtype=torch.int16, device=dev)
+        synth.dev_normal_bf16(self.x.data_ptr(), xo, seed + 7777, 0, 1.0)
+        self.x = self.x.view(torch.bfloat16)
+        self.y = torch.empty(yo, dtype=torch.bfloat16, device=dev)
+        wsb = max(q4.gemv_workspace_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
+        self.ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+        self.bytes_per_step = layers * sum(algo_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
+        self.weights_bytes = layers * sum(q4.weight_bytes(N, K) for _, N, K in LAYER_SHAPES)
+        self.launches_per_step = layers * len(LAYER_SHAPES)
+
+    def gemv(self, l: int, i: int, path=0):
+        _, N, K = LAYER_SHAPES[i]
+        q4 = self.q4
+        x = self.x[self.x_off[l][i]:self.x_off[l][i] + self.M * K].view(self.M, K)
+        y = self.y[self.y_off[l][i]:self.y_off[l][i] + self.M * N].view(self.M, N)
+        q4.gemv(x, self.qw[l][i], out=y, ws=self.ws, path=path)
+
+    def step(self, path=0):
+        for l in range(self.L):
+            for i in range(len(LAYER_SHAPES)):
+                self.gemv(l, i, path)
+
+
+def graph_of(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # eager warm-up (kernel attributes, plans)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, reps: int, warmup: int = 2) -> float:
+    """Average seconds per replay, CUDA events on the replaying stream."""
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        g.replay()
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b) / 1e3 / reps
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_sample(M: int, seed: int = 1000, rows_frac: int = 1):
+    """Layer 0 of the workload regenerated on the host and quantized by the
+    oracle (host threads).  Returns a list of (x, packed, scale, zero, N, K)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    o = oracle.load()
+    threads = os.cpu_count() or 1
+    out = []
+    for i, (_, N, K) in enumerate(LAYER_SHAPES):
+        n = N // rows_frac
+        W = np.empty((n, K), np.float32)
+        bounds = np.linspace(0, n, threads + 1).astype(int)
+
+        def gen(a, b):
+            W[a:b] = synth.normal_rows(seed + i, K, a, b, SIGMA)
+
+        ts = [threading.Thread(target=gen, args=(int(bounds[j]), int(bounds[j + 1])))
+              for j in range(threads)]
+        [t.start() for t in ts]
+        [t.join() for t in ts]
+        packed = np.empty((n, K // 2), np.uint8)
+        scale = np.empty((n, K // 128), np.float32)
+        zero = np.empty((n, K // 128), np.uint8)
+
+        def quant(a, b):
+            p, s, z = o.quantize(W[a:b])
+            packed[a:b], scale[a:b], zero[a:b] = p, s, z
+
+        ts = [threading.Thread(target=quant, args=(int(bounds[j]), int(bounds[j + 1])))
+              for j in range(threads) if bounds[j + 1] > bounds[j]]
+        [t.start() for t in ts]
+        [t.join() for t in ts]
+        del W
+        x = synth.bf16_bits_to_f32(synth.normal_bf16(seed + 7777 + i, 0, M * K)).reshape(M, K)
+        out.append((x, packed, scale, zero, n, K))
+    return out, threads
+
+
+def cpu_pass(sample, threads: int) -> tuple[float, int]:
+    import oracle
+    o = oracle.load()
+    t0 = time.perf_counter()
+    nbytes = 0
+    for (x, p, s, z, n, K) in sample:
+        o.dot_factored(x, p, s, z, n, K, threads=threads)
+        nbytes += algo_bytes(x.shape[0], n, K, xb=2, yb=2)
+    return time.perf_counter() - t0, nbytes
+
+
+# ------------------------------------------------------------------ main
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reference_arm(args, ws, rank):
+    """The oracle, as it stands, on the host cores: each step is one pass of
+    the page's factored dot over layer 0 of the workload (all four
+    matrices), regenerated and quantized on the host."""
+    if rank != 0:
+        return 0
+    sample, threads = cpu_sample(args.M)
+    for _ in range(args.warmup):
+        cpu_pass(sample, threads)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        t, b = cpu_pass(sample, threads)
+        tot_t += t
+        tot_b += b
+    gbs = tot_b / tot_t / 1e9
+    desc = (f"layer 0 of the 70B-shaped decode step (qkv, o, gate+up, down; "
+            f"{sum(p.shape[0] * p.shape[1] * 2 for (_, p, _, _, _, _) in sample) / 1e6:.0f} M "
+            f"weights), M={args.M}, f32 factored dot of the page, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"llama70b-shaped decode step, M={args.M}", "M": args.M,
+                       "layers_sampled": 1},
+            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=80)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 FMA, 2 MMA")
+    ap.add_argument("--no-rows", action="store_true", help="skip the extra measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="NxK: time one GEMV shape alone (small-case mode for profilers)")
+    ap.add_argument("--reps", type=int, default=3, help="launches in --case mode")
+    args = ap.parse_args()
+    if args.case:
+        return single_case(args)
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        return reference_arm(args, ws, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import weight_only_int4_group_gb300 as q4
+
+    pk = peaks()
+    work = Decode70B(q4, torch, args.M, args.layers)
+    g = graph_of(torch, lambda: work.step(args.path))
+
+    # ---- timed region: K replays of the decode-step graph
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    st = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        ev0.record(st)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(st)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    if ws > 1:
+        t = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+    assert q4.check() == q4.OK, "device error during the timed region"
+    clocks = clk.summary()
+
+    value = ws * work.bytes_per_step / t_step / 1e9
+    achieved = work.bytes_per_step / t_step / 1e9
+    traffic = profile_traffic("gemv_decode70b_M1.md", GEMV_SOURCES) if args.M == 1 else None
+
+    # ---- e2e: public API calls, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty(work.x_elems, dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(work.x.cpu())
+        hy = torch.empty(work.y_elems, dtype=torch.bfloat16, pin_memory=True)
+        reps = max(3, min(args.steps // 10, 20))
+        for _ in range(2):
+            work.x.copy_(hx, non_blocking=True)
+            work.step(args.path)
+            hy.copy_(work.y, non_blocking=True)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            work.x.copy_(hx, non_blocking=True)
+            work.step(args.path)
+            hy.copy_(work.y, non_blocking=True)
+        b.record(st)
+        b.synchronize()
+        t_e2e = a.elapsed_time(b) / 1e3 / reps
+        if ws > 1:
+            t = torch.tensor([t_e2e], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": round(ws * work.bytes_per_step / t_e2e / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": work.x_elems * 2, "d2h_bytes_per_step": work.y_elems * 2,
+               "ms_per_step": round(t_e2e * 1e3, 4), "api": "q4_gemv eager, 320 calls"}
+
+    # ---- extra measurements (rank 0 of a single-GPU run only)
+    rows = {}
+    if not args.no_rows and rank == 0:
+        rows = extra_rows(q4, torch, work, pk)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        sample, threads = cpu_sample(args.M)
+        tot_t, tot_b, passes = 0.0, 0, 0
+        while tot_t < 2.0 and passes < 50:
+            t, b = cpu_pass(sample, threads)
+            tot_t, tot_b, passes = tot_t + t, tot_b + b, passes + 1
+        cpu = {"value": round(tot_b / tot_t / 1e9, 3), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"layer 0 of the step (4 matrices, 855.6 M weights, host-generated "
+                         f"and oracle-quantized), M={args.M}, {passes} passes of the page's f32 "
+                         f"factored dot over {threads} threads, {tot_t:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"llama70b-shaped decode step: {args.layers} layers x "
+                                   f"(qkv 10240x8192, o 8192x8192, gate+up 57344x8192, "
+                                   f"down 8192x28672), M={args.M}",
+                       "M": args.M, "weights": "int4 asym group-128, f32 scale, u8 zero",
+                       "activations": "bf16", "outputs": "bf16", "accumulate": "f32",
+                       "weight_bytes_per_step": work.weights_bytes,
+                       "algorithmic_bytes_per_step": work.bytes_per_step,
+                       "us_per_token": round(t_step * 1e6, 2),
+                       "l2": "inputs (36.9 GB of weights) far larger than L2; no flush",
+                       "timing": "CUDA graph of the step, CUDA events on the replay stream",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": traffic, "peak_source": pk["source"],
+                         "kernel": "k_gemv (all 320 launches of the step)"},
+            "gpu_launches": work.launches_per_step * args.steps,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def extra_rows(q4, torch, work, pk) -> dict:
+    """Per-M sweep on the 70B MLP shapes (80 distinct weight copies, so no L2
+    reuse), the quantizer, and the large-M GEMM."""
+    rows = {}
+    sweep = {}
+    L = work.L
+    dev = torch.device("cuda")
+    for (name, N, K, mi) in (("up 28672x8192", 28672, 8192, 2), ("down 8192x28672", 8192, 28672, 3)):
+        # 28672x8192: the first 28672 rows of each fused gate+up weight (row tiles are outermost)
+        qws = []
+        for l in range(L):
+            base = work.qw[l][mi]
+            if base.N != N:
+                nb = q4.weight_bytes(N, K)
+                qws.append(q4.QWeight(base.data[:nb], N, K))
+            else:
+                qws.append(base)
+        res = {}
+        for M in (1, 2, 4, 8, 16):
+            x = torch.empty(M * K, dtype=torch.int16, device=dev)
+            import synth
+            synth.dev_normal_bf16(x.data_ptr(), M * K, 4242 + M, 0, 1.0)
+            x = x.view(torch.bfloat16).view(M, K)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsb = q4.gemv_workspace_bytes(M, N, K)
+            wsp = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+
+            def run():
+                for l in range(L):
+                    q4.gemv(x, qws[l], out=y, ws=wsp)
+            g = graph_of(torch, run)
+            t = time_graph(torch, g, reps=5) / L
+            b = algo_bytes(M, N, K)
+            res[f"M={M}"] = {"us_per_call": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                             "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4),
+                             "weight+scale GB/s": round((N * K // 2 + 5 * N * K // 128) / t / 1e9, 1),
+                             "TFLOP/s": round(2 * M * N * K / t / 1e12, 3)}
+            del g
+        sweep[name] = res
+    rows["mlp_sweep"] = sweep
+
+    # quantizer: HBM-bound, 4 B read + 0.539 B written per weight
+    N, K = 57344, 8192
+    import synth
+    w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    synth.dev_normal_f32(w.data_ptr(), N * K, 99, 0, SIGMA)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scale = torch.empty((N, K // 128), dtype=torch.float32, device=dev)
+    zero = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
+    lib = q4.lib()
+
+    def qrun():
+        lib.q4_quantize(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(), zero.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    g = graph_of(torch, qrun)
+    t = time_graph(torch, g, reps=10)
+    b = 4 * N * K + N * K // 2 + 5 * N * K // 128
+    rows["quantize"] = {"shape": f"{N}x{K} f32", "ms": round(t * 1e3, 3),
+                        "GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
+    del w, packed, scale, zero, g
+    torch.cuda.empty_cache()
+    return rows
+
+
+def single_case(args) -> int:
+    """One GEMV shape, `reps` launches on a few distinct weight copies (more
+    than L2 in total), printed as a plain JSON line.  Used to give profilers
+    a small, self-contained command."""
+    import torch
+
+    import synth
+    import weight_only_int4_group_gb300 as q4
+    N, K = (int(v) for v in args.case.lower().split("x"))
+    M = args.M
+    dev = torch.device("cuda")
+    copies = max(1, -(-3 * 129_000_000 // q4.weight_bytes(N, K)))  # >= 3x L2 in total
+    w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    qws = []
+    for c in range(copies):
+        synth.dev_normal_f32(w.data_ptr(), N * K, 500 + c, 0, SIGMA)
+        qws.append(q4.QWeight.from_float(w))
+    del w
+    x = torch.empty(M * K, dtype=torch.int16, device=dev)
+    synth.dev_normal_bf16(x.data_ptr(), M * K, 501, 0, 1.0)
+    x = x.view(torch.bfloat16).view(M, K)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = q4.workspace(M, N, K)
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(copies):  # warm-up: one launch per copy
+        q4.gemv(x, qws[i], out=y, ws=ws, path=args.path)
+    torch.cuda.synchronize()
+    a.record(st)
+    for i in range(args.reps):
+        q4.gemv(x, qws[i % copies], out=y, ws=ws, path=args.path)
+    b.record(st)
+    b.synchronize()
+    assert q4.check() == q4.OK
+    t = a.elapsed_time(b) / 1e3 / args.reps
+    nb = algo_bytes(M, N, K)
+    print(json.dumps({"case": f"{N}x{K}", "M": M, "path": args.path, "copies": copies,
+                      "launches": copies + args.reps, "us_per_call": round(t * 1e6, 2),
+                      "GB/s": round(nb / t / 1e9, 1)}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/q4.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
@@ -162,9 +164,10 @@ enum GemvPath { PATH_AUTO = 0, PATH_FMA = 1, PATH_MMA = 2 };
 
 struct GemvPlan {
     int path;
-    int rb;      // row tiles per CTA
+    int rb;      // row tiles per unit
     int ks, gs;  // K slices, groups per slice
     int nrb;     // row blocks
+    int grid;    // persistent CTAs
     size_t workspace;
 };
 
