@@ -513,6 +513,22 @@ def extra_rows(q4, torch, work, pk) -> dict:
                              "weight+scale GB/s": round((N * K // 2 + 5 * N * K // 128) / t / 1e9, 1),
                              "TFLOP/s": round(2 * M * N * K / t / 1e12, 3)}
             del g
+        # M = 1 through each kernel explicitly (AUTO picks the tensor-core one)
+        x = torch.empty(K, dtype=torch.int16, device=dev)
+        synth.dev_normal_bf16(x.data_ptr(), K, 4242, 0, 1.0)
+        x = x.view(torch.bfloat16).view(1, K)
+        y = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+        wsp = torch.zeros(max(q4.gemv_workspace_bytes(1, N, K), 256), dtype=torch.uint8, device=dev)
+        for pname, pid in (("M=1 cuda-core FMA", q4.PATH_FMA), ("M=1 tensor-core MMA", q4.PATH_MMA)):
+            def runp():
+                for l in range(L):
+                    q4.gemv(x, qws[l], out=y, ws=wsp, path=pid)
+            g = graph_of(torch, runp)
+            t = time_graph(torch, g, reps=5) / L
+            b = algo_bytes(1, N, K)
+            res[pname] = {"us_per_call": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                          "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
+            del g
         sweep[name] = res
     rows["mlp_sweep"] = sweep
 

@@ -139,10 +139,11 @@ q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
                   void *y, q4_dtype yt, void *workspace, size_t workspace_bytes,
                   q4_stream_t stream);
 
-/* Kernel choice for q4_gemv_path: AUTO is what q4_gemv uses (FMA for M = 1,
- * MMA otherwise).  FMA: CUDA-core f32 FMAs on codes turned into f32 in
- * registers (M = 1 only).  MMA: m16n8k16 tensor-core MMAs with the codes as
- * bf16/f16 A fragments built in registers and the batch as the n dimension. */
+/* Kernel choice for q4_gemv_path.  FMA: CUDA-core f32 FMAs on codes turned
+ * into f32 in registers (M = 1 only).  MMA: m16n8k16 tensor-core MMAs with the
+ * codes as bf16/f16 A fragments built in registers and the batch as the n
+ * dimension.  AUTO (what q4_gemv uses): MMA, except FMA for f32 activations
+ * at M = 1. */
 #define Q4_PATH_AUTO 0
 #define Q4_PATH_FMA 1
 #define Q4_PATH_MMA 2

@@ -90,9 +90,8 @@ static q4_status gemv_common(const void *x, q4_dtype xt, int64_t M, int64_t N, i
     a.qw = static_cast<const uint8_t *>(qw);
     a.y = y;
     a.yt = yt;
-    a.ks = plan.ks;
-    a.gs = plan.gs;
-    if (plan.ks > 1) {
+    a.maxc = plan.maxc;
+    if (plan.maxc > 1) {
         a.count = static_cast<unsigned int *>(workspace);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                               counters_bytes(plan.nrb));
@@ -165,8 +164,10 @@ size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K)
     const GemvPlan a = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                                  Q4_BF16, PATH_AUTO, d->sm_count);
     const GemvPlan b = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                 Q4_BF16, M == 1 ? PATH_MMA : PATH_AUTO, d->sm_count);
-    return a.workspace > b.workspace ? a.workspace : b.workspace;
+                                 Q4_F32, PATH_AUTO, d->sm_count);
+    const GemvPlan c = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                 Q4_F32, M == 1 ? PATH_FMA : PATH_MMA, d->sm_count);
+    return std::max(a.workspace, std::max(b.workspace, c.workspace));
 }
 
 q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,

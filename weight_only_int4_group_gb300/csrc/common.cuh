@@ -152,9 +152,9 @@ struct GemvArgs {
     const uint8_t *qw;
     void *y;
     q4_dtype yt;
-    float *partial;       // [KS][M][ntiles*16] when KS > 1
-    unsigned int *count;  // [nrb] split-K arrival counters when KS > 1
-    int ks, gs;           // number of K slices, groups per slice
+    float *partial;       // [nrb][maxc][64 rows][M] partial sums of shared row blocks
+    unsigned int *count;  // [nrb] arrival counters of shared row blocks
+    int maxc;             // most CTAs that share one row block
     uint64_t wait_ns;     // bound of every mbarrier wait
     unsigned int *err;    // device error word
     int debug_no_copy;    // producer issues no copy (exercises the timeout path)
@@ -164,15 +164,15 @@ enum GemvPath { PATH_AUTO = 0, PATH_FMA = 1, PATH_MMA = 2 };
 
 struct GemvPlan {
     int path;
-    int rb;      // row tiles per unit
-    int ks, gs;  // K slices, groups per slice
-    int nrb;     // row blocks
-    int grid;    // persistent CTAs
+    int rb;    // row tiles per row block
+    int nrb;   // row blocks
+    int grid;  // persistent CTAs
+    int maxc;  // most CTAs sharing one row block (1: no partial sums)
     size_t workspace;
 };
 
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
-size_t counters_bytes(int nrb);  // split-K counter block at the start of the workspace
+size_t counters_bytes(int nrb);  // counter block at the start of the workspace
 cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,

@@ -6,73 +6,77 @@
 // sections "How it works" and "Code", function `dot`), with the 4-bit codes
 // turned into floating point in registers and never written back to memory.
 //
-// Structure: a persistent kernel, one CTA = 4 consumer warps + 1 producer
-// warp, a few CTAs per SM.  The work is cut into units of RB = 4 row tiles
-// (64 output rows) by one slice of groups along K; CTA c takes units c,
-// c + grid, c + 2*grid, ...  The producer warp walks the same sequence and
-// streams, with 1-D bulk asynchronous copies (TMA engine), the weight tiles
-// into a 4-stage shared-memory ring (stage = RB row tiles x 4 consecutive
-// groups) -- it runs ahead across unit boundaries, so the memory pipeline
-// never drains between units.  Consumer warp w takes group w of every stage.
-// Partial sums are reduced across warps in shared memory and, when K is split
-// over several units, across slices through a workspace by the last unit of
-// the row block to finish (fixed summation order: results do not depend on
-// timing).
+// Work decomposition (stream-K): the output rows are cut into row blocks of
+// RB = 4 tiles (64 rows); each row block is a sequence of NS = ceil(NG/4)
+// steps, a step being 4 consecutive groups along K.  The nrb * NS items are
+// split into `grid` contiguous, equal ranges, one per persistent CTA (a few
+// CTAs per SM).  A CTA accumulates the steps of a row block in registers and
+// writes the row block out when it reaches its last step; a row block whose
+// steps are spread over several CTAs is finished by the last of them to
+// arrive, which sums the partial results in CTA order (so results do not
+// depend on timing).
+//
+// CTA = 4 consumer warps + 1 producer warp.  The producer streams each step's
+// weight tiles (RB row tiles x 4 groups) with 1-D bulk asynchronous copies
+// (TMA engine) into a 3-stage shared-memory ring and runs ahead across row
+// blocks, so the memory pipeline never drains.  Consumer warp w takes group w
+// of every step.
 //
 // Two consumer variants:
 //   FMA (M = 1): CUDA-core path.  A 4-bit code q at bit offset 16 or 12 of a
 //     word becomes the f32 value 1 + q/128 or 1 + q/2048 with one LOP3
 //     (mantissa bits under the exponent of 1.0); two such values are
 //     multiplied into a pair of f32 accumulators by one packed FFMA2.  The
-//     constant 1 is removed per group with the activation sums.  The
-//     producer also copies each unit's activation slice into a double-buffered
-//     shared-memory slot; the consumers turn it into the per-lane pair order
-//     once per unit.
+//     constant 1 is removed per group with the activation sums.  The step's
+//     activations ride in the same stage; each warp turns its group's into
+//     the per-lane pair order.
 //   MMA (M = 1..16, bf16/f16 activations; f32 activations as bf16 hi + lo):
 //     each word yields the four A-fragment registers of an m16n8k16
 //     tensor-core MMA as bf16 pairs 128 + q (f16: 1024 + q) with one LOP3
 //     each; the activations are the B fragment (the batch is the MMA's n
-//     dimension).  The group sums of the activations come from one extra MMA
-//     per k-step with an all-ones A operand, once per group.  Per group,
-//     y += scale * (D - (offset + zero) * sum x).
+//     dimension).  For M <= 8 (bf16/f16) the producer copies the step's
+//     activation rows into the stage next to the tiles (rows padded by 16
+//     bytes so the eight batch rows fall in different banks); otherwise each
+//     lane loads its B fragments from L2 one step ahead.  The group sums of the
+//     activations come from one extra MMA per k-step with an all-ones A
+//     operand.  Per group, y += scale * (D - (offset + zero) * sum x).
 #include "common.cuh"
 
 namespace q4 {
 
-constexpr int W = 4;        // consumer warps
-constexpr int RB = 4;       // row tiles per unit
+constexpr int W = 4;        // consumer warps = groups per step
+constexpr int RB = 4;       // row tiles per row block
 constexpr int NSTAGE = 3;   // ring depth
 constexpr int THREADS = (W + 1) * 32;
 constexpr int CONSUMERS = W * 32;
-constexpr int STAGE_BYTES = RB * W * TILE_BYTES;  // 17664
-constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;  // 52992
+constexpr int TILES_BYTES = RB * W * TILE_BYTES;  // 17664
+constexpr int XSTAGE_BYTES = W * G * 4;           // FMA: the step's activations (f32 worst case)
 constexpr int CTRL_BYTES = 128;                   // barriers + flags
-constexpr int GS_MAX_FMA = 8;
-constexpr int GS_MAX_MMA = 32;
-// FMA activation pairs: one record of 64 floats per (group, lane class t),
-// padded to 68 floats so the four lane classes of a warp read four different
-// bank groups in the same wavefront.
+// FMA activation pairs, per warp: one record of 64 floats per lane class t,
+// padded to 68 floats so the four lane classes read four different bank
+// groups in one wavefront; then the four sum records.
 constexpr int PAIR_STRIDE = 68;
-constexpr int FMA_XSLOT_BYTES = GS_MAX_FMA * G * 4;  // one unit's activations (f32 worst case)
-constexpr int FMA_PAIR_FLOATS = GS_MAX_FMA * 4 * PAIR_STRIDE;
-constexpr int FMA_PAIR_BYTES = FMA_PAIR_FLOATS * 4 + GS_MAX_FMA * 4 * 16;
+constexpr int WARP_PAIR_FLOATS = 4 * PAIR_STRIDE + 4 * 4;
 constexpr int RED_FLOATS_FMA = W * RB * 16;
-constexpr int RED_FLOATS_MMA = W * RB * 16 * 16;
 constexpr int MIN_BLOCKS = 3;  // CTAs per SM the shared memory budget is sized for
 
-static_assert(RING_BYTES % 128 == 0, "ring alignment");
-static_assert(MIN_BLOCKS * (RING_BYTES + CTRL_BYTES + 2 * FMA_XSLOT_BYTES + FMA_PAIR_BYTES +
-                            RED_FLOATS_FMA * 4 + 1024) <= 228 * 1024,
-              "three FMA CTAs per SM");
-static_assert(MIN_BLOCKS * (RING_BYTES + CTRL_BYTES + RED_FLOATS_MMA * 4 + 1024) <= 228 * 1024,
-              "three MMA CTAs per SM");
+constexpr int XROW = W * G * 2 + 16;  // MMA staged activations: one padded row per batch row
 
-__host__ __device__ constexpr int smem_bytes(int mode)
+// xrows: batch rows staged with each step (MMA, M <= 8); 0 otherwise
+__host__ __device__ constexpr int stage_bytes(int mode, int xrows)
 {
-    return mode == PATH_FMA
-               ? RING_BYTES + CTRL_BYTES + 2 * FMA_XSLOT_BYTES + FMA_PAIR_BYTES + RED_FLOATS_FMA * 4
-               : RING_BYTES + CTRL_BYTES + RED_FLOATS_MMA * 4;
+    return mode == PATH_FMA ? TILES_BYTES + XSTAGE_BYTES
+                            : ((TILES_BYTES + xrows * XROW + 127) / 128) * 128;
 }
+
+__host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms)
+{
+    return NSTAGE * stage_bytes(mode, xrows) + CTRL_BYTES +
+           (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4);
+}
+
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "three FMA CTAs per SM");
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 1, 8) + 1024) <= 228 * 1024, "three MMA CTAs per SM");
 
 __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float v)
 {
@@ -82,13 +86,6 @@ __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float
         static_cast<__nv_bfloat16 *>(y)[idx] = __float2bfloat16_rn(v);
     else
         static_cast<__half *>(y)[idx] = __float2half_rn(v);
-}
-
-// (1 + q_hi/128, 1 + q_lo/2048) from the codes at bit offsets 16 and 12.
-__device__ __forceinline__ float2 code_pair(uint32_t v)
-{
-    return make_float2(__uint_as_float(lop3_and_or(v, 0x000F0000u, 0x3F800000u)),
-                       __uint_as_float(lop3_and_or(v, 0x0000F000u, 0x3F800000u)));
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -138,21 +135,66 @@ __device__ __forceinline__ float smem_x_f32(const uint8_t *xs, q4_dtype xt, int 
     return __half2float(__half(hr));
 }
 
-struct UnitInfo {
-    int rb, ks, rt0, nrt, g_begin, g_end, nsteps;
-};
 
-__device__ __forceinline__ UnitInfo unit_info(const GemvArgs &a, int u, int ntiles, int NG)
+// One word -> the four A-fragment registers (bf16 128 + q or f16 1024 + q
+// pairs: one shift and one LOP3 each) -> one m16n8k16 MMA into d.  Written as
+// a single PTX block so the fragment registers are allocated in place.
+template <int ABT>
+__device__ __forceinline__ void mma_word(float (&d)[4], uint32_t w, uint32_t b0, uint32_t b1)
 {
-    UnitInfo ui;
-    ui.ks = u % a.ks;
-    ui.rb = u / a.ks;
-    ui.rt0 = ui.rb * RB;
-    ui.nrt = min(RB, ntiles - ui.rt0);
-    ui.g_begin = ui.ks * a.gs;
-    ui.g_end = min(NG, ui.g_begin + a.gs);
-    ui.nsteps = (ui.g_end - ui.g_begin + W - 1) / W;
-    return ui;
+    if (ABT == 0)
+        asm("{\n\t.reg .b32 t1, t2, t3, a0, a1, a2, a3;\n\t"
+            "shr.b32 t1, %4, 4;\n\tshr.b32 t2, %4, 8;\n\tshr.b32 t3, %4, 12;\n\t"
+            "lop3.b32 a0, %4, 0x000F000F, 0x43004300, 0xEA;\n\t"
+            "lop3.b32 a1, t1, 0x000F000F, 0x43004300, 0xEA;\n\t"
+            "lop3.b32 a3, t2, 0x000F000F, 0x43004300, 0xEA;\n\t"
+            "lop3.b32 a2, t3, 0x000F000F, 0x43004300, 0xEA;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3}, {%5,%6}, {%0,%1,%2,%3};\n\t}"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(w), "r"(b0), "r"(b1));
+    else
+        asm("{\n\t.reg .b32 t1, t2, t3, a0, a1, a2, a3;\n\t"
+            "shr.b32 t1, %4, 4;\n\tshr.b32 t2, %4, 8;\n\tshr.b32 t3, %4, 12;\n\t"
+            "lop3.b32 a0, %4, 0x000F000F, 0x64006400, 0xEA;\n\t"
+            "lop3.b32 a1, t1, 0x000F000F, 0x64006400, 0xEA;\n\t"
+            "lop3.b32 a3, t2, 0x000F000F, 0x64006400, 0xEA;\n\t"
+            "lop3.b32 a2, t3, 0x000F000F, 0x64006400, 0xEA;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3}, {%5,%6}, {%0,%1,%2,%3};\n\t}"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(w), "r"(b0), "r"(b1));
+}
+
+// One word (and the next word of its 16-byte chunk, for the funnel step) ->
+// four packed FFMA2 steps: code pairs from bit offsets (16, 12) of w, w >> 8,
+// w << 8 and the funnel (w_next:w) >> 16, each made with two LOP3s.
+__device__ __forceinline__ void fma_word(float2 &aG, float2 &aG8, uint32_t w, uint32_t wn,
+                                         float2 p0, float2 p1, float2 p2, float2 p3)
+{
+    asm("{\n\t.reg .b32 r8, l8, fu, l, h;\n\t.reg .b64 v, x, g, g8;\n\t"
+        "mov.b64 g, {%0, %1};\n\tmov.b64 g8, {%2, %3};\n\t"
+        "shr.b32 r8, %4, 8;\n\tshl.b32 l8, %4, 8;\n\tshf.r.clamp.b32 fu, %4, %5, 16;\n\t"
+        "lop3.b32 l, %4, 0x000F0000, 0x3F800000, 0xEA;\n\tlop3.b32 h, %4, 0x0000F000, 0x3F800000, 0xEA;\n\t"
+        "mov.b64 v, {l, h};\n\tmov.b64 x, {%6, %7};\n\tfma.rn.f32x2 g, v, x, g;\n\t"
+        "lop3.b32 l, r8, 0x000F0000, 0x3F800000, 0xEA;\n\tlop3.b32 h, r8, 0x0000F000, 0x3F800000, 0xEA;\n\t"
+        "mov.b64 v, {l, h};\n\tmov.b64 x, {%8, %9};\n\tfma.rn.f32x2 g8, v, x, g8;\n\t"
+        "lop3.b32 l, l8, 0x000F0000, 0x3F800000, 0xEA;\n\tlop3.b32 h, l8, 0x0000F000, 0x3F800000, 0xEA;\n\t"
+        "mov.b64 v, {l, h};\n\tmov.b64 x, {%10, %11};\n\tfma.rn.f32x2 g8, v, x, g8;\n\t"
+        "lop3.b32 l, fu, 0x000F0000, 0x3F800000, 0xEA;\n\tlop3.b32 h, fu, 0x0000F000, 0x3F800000, 0xEA;\n\t"
+        "mov.b64 v, {l, h};\n\tmov.b64 x, {%12, %13};\n\tfma.rn.f32x2 g, v, x, g;\n\t"
+        "mov.b64 {%0, %1}, g;\n\tmov.b64 {%2, %3}, g8;\n\t}"
+        : "+f"(aG.x), "+f"(aG.y), "+f"(aG8.x), "+f"(aG8.y)
+        : "r"(w), "r"(wn), "f"(p0.x), "f"(p0.y), "f"(p1.x), "f"(p1.y), "f"(p2.x), "f"(p2.y),
+          "f"(p3.x), "f"(p3.y));
+}
+
+// First item of CTA c, and the CTA that owns item i, for T items over G CTAs.
+__host__ __device__ __forceinline__ int64_t range_begin(int64_t c, int64_t T, int64_t G)
+{
+    return c * T / G;
+}
+__host__ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64_t G)
+{
+    return ((i + 1) * G - 1) / T;
 }
 
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
@@ -160,36 +202,34 @@ __device__ __forceinline__ UnitInfo unit_info(const GemvArgs &a, int u, int ntil
 template <int MODE, int NT, int ABT, bool XSPLIT>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
+    constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    const int xrows = XSTAGED ? a.M : 0;
+    const int SB = stage_bytes(MODE, xrows);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * SB);
     uint64_t *empty = full + NSTAGE;
-    uint64_t *xfull = empty + NSTAGE;  // FMA activation slots
-    uint64_t *xempty = xfull + 2;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(xempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NSTAGE);
     int *last_flag = const_cast<int *>(abort_flag) + 1;
-    uint8_t *after = smem + RING_BYTES + CTRL_BYTES;
-    uint8_t *xslot = after;                                                 // FMA: 2 slots
-    float *pairs = reinterpret_cast<float *>(after + 2 * FMA_XSLOT_BYTES);  // FMA
-    float *red = (MODE == PATH_FMA)
-                     ? reinterpret_cast<float *>(after + 2 * FMA_XSLOT_BYTES + FMA_PAIR_BYTES)
-                     : reinterpret_cast<float *>(after);
+    float *after = reinterpret_cast<float *>(smem + NSTAGE * SB + CTRL_BYTES);
+    float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
+    constexpr int MSR = (MODE == PATH_FMA) ? 1 : 8 * NT;  // red row stride
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
+    const int NS = (NG + W - 1) / W;
     const int ntiles = (a.N + TILE_ROWS - 1) / TILE_ROWS;
     const int nrb = (ntiles + RB - 1) / RB;
-    const int U = nrb * a.ks;
+    const int64_t T = static_cast<int64_t>(nrb) * NS;
+    const int64_t Gc = gridDim.x;
+    const int64_t beg = range_begin(blockIdx.x, T, Gc);
+    const int64_t end = range_begin(blockIdx.x + 1, T, Gc);
     const int xb = (a.xt == Q4_F32) ? 4 : 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], W);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&xfull[s], 1);
-            mbar_init(&xempty[s], W);
         }
         *abort_flag = 0;
         *last_flag = 0;
@@ -200,55 +240,41 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // ------------------------------------------------------------ producer
     if (warp == W) {
         if (lane == 0) {
-            int gstep = 0, ui = 0, xissued = 0;
-            bool ok = true;
+            int gstep = 0;
             if (!a.debug_no_copy) {
-                for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++ui) {
-                    const UnitInfo un = unit_info(a, u, ntiles, NG);
-                    if (MODE == PATH_FMA) {
-                        const int xs = ui & 1;
-                        if (ui >= 2 && !mbar_wait_bounded(&xempty[xs], ((ui >> 1) - 1) & 1,
-                                                          abort_flag, a.wait_ns, a.err)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t bytes =
-                            static_cast<uint32_t>(un.g_end - un.g_begin) * G * xb;
-                        mbar_arrive_expect_tx(&xfull[xs], bytes);
-                        bulk_g2s(xslot + xs * FMA_XSLOT_BYTES,
+                for (int64_t it = beg; it < end; ++it, ++gstep) {
+                    const int rb = static_cast<int>(it / NS), s = static_cast<int>(it % NS);
+                    const int slot = gstep % NSTAGE;
+                    if (gstep >= NSTAGE &&
+                        !mbar_wait_bounded(&empty[slot], ((gstep / NSTAGE) - 1) & 1, abort_flag,
+                                           a.wait_ns, a.err))
+                        break;
+                    const int rt0 = rb * RB, nrt = min(RB, ntiles - rt0);
+                    const int g0 = s * W, ng = min(W, NG - g0);
+                    const uint32_t row_bytes = static_cast<uint32_t>(ng) * TILE_BYTES;
+                    const uint32_t xbytes = (MODE == PATH_FMA) ? static_cast<uint32_t>(ng) * G * xb
+                                            : static_cast<uint32_t>(xrows) * ng * G * 2;
+                    uint8_t *stage = ring + slot * SB;
+                    mbar_arrive_expect_tx(&full[slot], row_bytes * nrt + xbytes);
+                    for (int r = 0; r < nrt; ++r)
+                        bulk_g2s(stage + r * W * TILE_BYTES,
+                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g0) * TILE_BYTES,
+                                 row_bytes, &full[slot]);
+                    if (MODE == PATH_FMA)
+                        bulk_g2s(stage + TILES_BYTES,
+                                 static_cast<const uint8_t *>(a.x) + static_cast<int64_t>(g0) * G * xb,
+                                 xbytes, &full[slot]);
+                    for (int m = 0; m < xrows; ++m)
+                        bulk_g2s(stage + TILES_BYTES + m * XROW,
                                  static_cast<const uint8_t *>(a.x) +
-                                     static_cast<int64_t>(un.g_begin) * G * xb,
-                                 bytes, &xfull[xs]);
-                        ++xissued;
-                    }
-                    for (int ps = 0; ps < un.nsteps; ++ps, ++gstep) {
-                        const int slot = gstep % NSTAGE;
-                        if (gstep >= NSTAGE &&
-                            !mbar_wait_bounded(&empty[slot], ((gstep / NSTAGE) - 1) & 1,
-                                               abort_flag, a.wait_ns, a.err)) {
-                            ok = false;
-                            break;
-                        }
-                        const int g0 = un.g_begin + ps * W;
-                        const int ng = min(W, un.g_end - g0);
-                        const uint32_t row_bytes = static_cast<uint32_t>(ng) * TILE_BYTES;
-                        mbar_arrive_expect_tx(&full[slot], row_bytes * un.nrt);
-                        for (int r = 0; r < un.nrt; ++r) {
-                            const uint8_t *src =
-                                a.qw + (static_cast<int64_t>(un.rt0 + r) * NG + g0) * TILE_BYTES;
-                            bulk_g2s(ring + slot * STAGE_BYTES + r * W * TILE_BYTES, src,
-                                     row_bytes, &full[slot]);
-                        }
-                    }
+                                     (static_cast<int64_t>(m) * a.K + static_cast<int64_t>(g0) * G) * 2,
+                                 static_cast<uint32_t>(ng) * G * 2, &full[slot]);
                 }
             }
             // Every issued copy must land before the CTA may exit.
             for (int s = max(0, gstep - NSTAGE); s < gstep; ++s)
                 mbar_wait_bounded(&full[s % NSTAGE], (s / NSTAGE) & 1, abort_flag, a.wait_ns,
                                   a.err, false);
-            for (int i = max(0, xissued - 2); i < xissued; ++i)
-                mbar_wait_bounded(&xfull[i & 1], (i >> 1) & 1, abort_flag, a.wait_ns, a.err,
-                                  false);
         }
         return;
     }
@@ -256,234 +282,219 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // ------------------------------------------------------------ consumers
     const int gq = lane >> 2, t = lane & 3;
     const int M = a.M;
-    const int MS = (MODE == PATH_FMA) ? 1 : 16;
+    const int MS = MSR;
     const int Mo = (MODE == PATH_FMA) ? 1 : M;
-    const int npad = ntiles * TILE_ROWS;
-    int gstep = 0, ui = 0;
-    bool ok = true;
+    float *mypairs = after + warp * WARP_PAIR_FLOATS;  // FMA
 
-    for (int u = blockIdx.x; u < U; u += gridDim.x, ++ui) {
-        const UnitInfo un = unit_info(a, u, ntiles, NG);
-
-        if (MODE == PATH_FMA) {
-            // Activation pairs in the order the code fields are extracted (see
-            // the word layout in q4.h): per word, (x1,x8) (x9,x1) (x8,x0)
-            // (x0',x9) with xa = x[16j + 2t + a] and x0' from the next word of
-            // the same 16-byte chunk; plus S = sum x and the two offset terms.
-            const int xs = ui & 1;
-            ok = mbar_wait_bounded(&xfull[xs], (ui >> 1) & 1, abort_flag, a.wait_ns, a.err);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            const uint8_t *xsrc = xslot + xs * FMA_XSLOT_BYTES;
-            const int ngs = un.g_end - un.g_begin;
-            // record (gl, tt, j): one word's 8 pair floats; 32 records per
-            // group, so every warp-wide pass covers whole (gl, tt) octets
-            for (int base = 0; base < ngs * 32; base += CONSUMERS) {
-                const int rec = base + threadIdx.x;
-                const bool live = rec < ngs * 32;
-                const int gl = rec >> 5, tt = (rec >> 3) & 3, j = rec & 7;
-                const int jn = (j & 4) | ((j + 1) & 3);
-                const int kb = gl * G + 2 * tt;
-                float x0 = 0.0f, x1 = 0.0f, x8 = 0.0f, x9 = 0.0f, x0n = 0.0f;
-                if (live) {
-                    x0 = smem_x_f32(xsrc, a.xt, kb + 16 * j);
-                    x1 = smem_x_f32(xsrc, a.xt, kb + 16 * j + 1);
-                    x8 = smem_x_f32(xsrc, a.xt, kb + 16 * j + 8);
-                    x9 = smem_x_f32(xsrc, a.xt, kb + 16 * j + 9);
-                    x0n = smem_x_f32(xsrc, a.xt, kb + 16 * jn);
-                    float4 *dst = reinterpret_cast<float4 *>(pairs + (gl * 4 + tt) * PAIR_STRIDE + 8 * j);
-                    dst[0] = make_float4(x1, x8, x9, x1);
-                    dst[1] = make_float4(x8, x0, x0n, x9);
+    // MMA: the warp's B fragments for the current step, the next step's
+    // prefetched while the current one computes (f32 hi/lo: loaded per step)
+    constexpr bool PREFETCH = (MODE == PATH_MMA) && !XSPLIT && !XSTAGED;
+    uint32_t bcur[NT][8][2], bnxt[PREFETCH ? NT : 1][8][2], blo[XSPLIT ? NT : 1][8][2];
+    auto load_b = [&](int gg, uint32_t (&bh)[NT][8][2], uint32_t (&bl)[XSPLIT ? NT : 1][8][2]) {
+        const bool act = gg < NG;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int m = 8 * n + gq;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int64_t k = static_cast<int64_t>(gg) * G + 16 * j + 2 * t;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t vh = 0, vl = 0;
+                    if (act && m < M) {
+                        const int64_t idx = static_cast<int64_t>(m) * a.K + k + 8 * h;
+                        if (XSPLIT) {
+                            const float2 xv = __ldg(reinterpret_cast<const float2 *>(
+                                static_cast<const float *>(a.x) + idx));
+                            vh = pack_bf16x2(xv.x, xv.y);
+                            vl = pack_bf16x2(xv.x - bf16_lo_f32(vh), xv.y - bf16_hi_f32(vh));
+                        } else {
+                            vh = __ldg(reinterpret_cast<const unsigned int *>(
+                                static_cast<const uint16_t *>(a.x) + idx));
+                        }
+                    }
+                    bh[n][j][h] = vh;
+                    if (XSPLIT) bl[XSPLIT ? n : 0][j][h] = vl;
                 }
-                // sums over the 8 words of this (gl, tt): lanes 8i..8i+7 share it
+            }
+        }
+    };
+    if (MODE == PATH_MMA && !XSTAGED && beg < end)
+        load_b(static_cast<int>(beg % NS) * W + warp, bcur, blo);
+
+    float yacc[RB][NT][4];
+    int gstep = 0;
+    bool ok = true;
+    for (int64_t it = beg; it < end; ++it, ++gstep) {
+        const int rb = static_cast<int>(it / NS), s = static_cast<int>(it % NS);
+        const int slot = gstep % NSTAGE;
+        const int g = s * W + warp;
+        const bool active = g < NG;
+        const int nrt = min(RB, ntiles - rb * RB);
+        if (it == beg || s == 0) {
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) yacc[r][n][e] = 0.0f;
+        }
+
+        ok = mbar_wait_bounded(&full[slot], (gstep / NSTAGE) & 1, abort_flag, a.wait_ns, a.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+        }
+        if (MODE == PATH_MMA && XSPLIT && it > beg) load_b(g, bcur, blo);
+        if (PREFETCH && it + 1 < end)
+            load_b(static_cast<int>((it + 1) % NS) * W + warp,
+                   reinterpret_cast<uint32_t (&)[NT][8][2]>(bnxt), blo);
+        const uint8_t *stage = ring + slot * SB;
+        const uint8_t *wtiles = stage + warp * TILE_BYTES;
+        if (XSTAGED) {
+            const uint8_t *xs = stage + TILES_BYTES + gq * XROW + warp * G * 2 + 4 * t;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    bcur[0][j][h] = (gq < M && active)
+                                        ? *reinterpret_cast<const uint32_t *>(xs + 32 * j + 16 * h)
+                                        : 0u;
+        }
+
+        if (active && MODE == PATH_FMA) {
+            // This warp's group activations -> pair records.  Lane (tt, j)
+            // writes word j of lane class tt: (x1,x8) (x9,x1) (x8,x0)
+            // (x0',x9) with xa = x[16j + 2tt + a] and x0' from the next word
+            // of the same 16-byte chunk (see the word layout in q4.h).
+            {
+                const int tt = lane >> 3, j = lane & 7;
+                const int jn = (j & 4) | ((j + 1) & 3);
+                const uint8_t *xs = stage + TILES_BYTES;
+                const int kb = warp * G + 2 * tt;
+                const float x0 = smem_x_f32(xs, a.xt, kb + 16 * j);
+                const float x1 = smem_x_f32(xs, a.xt, kb + 16 * j + 1);
+                const float x8 = smem_x_f32(xs, a.xt, kb + 16 * j + 8);
+                const float x9 = smem_x_f32(xs, a.xt, kb + 16 * j + 9);
+                const float x0n = smem_x_f32(xs, a.xt, kb + 16 * jn);
+                float4 *dst = reinterpret_cast<float4 *>(mypairs + tt * PAIR_STRIDE + 8 * j);
+                dst[0] = make_float4(x1, x8, x9, x1);
+                dst[1] = make_float4(x8, x0, x0n, x9);
                 float slo = x0 + x1, shi = x8 + x9;
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) {
                     slo += __shfl_xor_sync(0xffffffffu, slo, o);
                     shi += __shfl_xor_sync(0xffffffffu, shi, o);
                 }
-                if (live && j == 0)
-                    reinterpret_cast<float4 *>(pairs + FMA_PAIR_FLOATS)[gl * 4 + tt] =
+                if (j == 0)
+                    reinterpret_cast<float4 *>(mypairs + 4 * PAIR_STRIDE)[tt] =
                         make_float4(slo + shi, 128.0f * slo + 2048.0f * shi,
                                     128.0f * shi + 2048.0f * slo, 0.0f);
             }
-            named_barrier_sync(1, CONSUMERS);
-            if (lane == 0) mbar_arrive(&xempty[xs]);
-        }
-
-        float yacc[RB][NT][4];
+            __syncwarp();
+            const float4 *xpp = reinterpret_cast<const float4 *>(mypairs + t * PAIR_STRIDE);
+            float2 P[8][4];
 #pragma unroll
-        for (int r = 0; r < RB; ++r)
+            for (int j = 0; j < 8; ++j) {
+                const float4 p = xpp[2 * j], q = xpp[2 * j + 1];
+                P[j][0] = make_float2(p.x, p.y);
+                P[j][1] = make_float2(p.z, p.w);
+                P[j][2] = make_float2(q.x, q.y);
+                P[j][3] = make_float2(q.z, q.w);
+            }
+            const float4 xsv = reinterpret_cast<const float4 *>(mypairs + 4 * PAIR_STRIDE)[t];
+            // all RB tiles at once: RB independent accumulator chains
+            uint32_t wv[RB][8];
+            float2 sp[RB];
+            uint32_t zp[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const uint8_t *tile = wtiles + r * W * TILE_BYTES;
+                const bool live = r < nrt;
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
+                sp[r] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
+                zp[r] = *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq);
+                wv[r][0] = c0.x; wv[r][1] = c0.y; wv[r][2] = c0.z; wv[r][3] = c0.w;
+                wv[r][4] = c1.x; wv[r][5] = c1.y; wv[r][6] = c1.z; wv[r][7] = c1.w;
+            }
+            float2 accG[RB], accG8[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                accG[r] = make_float2(0.0f, 0.0f);
+                accG8[r] = make_float2(0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                for (int r = 0; r < RB; ++r) {
+                    fma_word(accG[r], accG8[r], wv[r][j], wv[r][(j & 4) | ((j + 1) & 3)], P[j][0],
+                             P[j][1], P[j][2], P[j][3]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const float zg = static_cast<float>(zp[r] & 0xFFu);
+                const float zg8 = static_cast<float>(zp[r] >> 8);
+                const float ig =
+                    fmaf(128.0f, accG[r].x, fmaf(2048.0f, accG[r].y, -fmaf(zg, xsv.x, xsv.y)));
+                const float ig8 =
+                    fmaf(128.0f, accG8[r].x, fmaf(2048.0f, accG8[r].y, -fmaf(zg8, xsv.x, xsv.z)));
+                yacc[r][0][0] = fmaf(sp[r].x, ig, yacc[r][0][0]);
+                yacc[r][0][2] = fmaf(sp[r].y, ig8, yacc[r][0][2]);
+            }
+        } else if (active && MODE == PATH_MMA) {
+            const uint32_t MAG = ABT == 0 ? 0x43004300u : 0x64006400u;
+            const uint32_t ONES = ABT == 0 ? 0x3F803F80u : 0x3C003C00u;
+            const float OFF = ABT == 0 ? 128.0f : 1024.0f;
+            // TI tiles at a time: TI * NT independent accumulator chains, plus
+            // NT chains for the activation sums
+            constexpr int TI = (NT == 1) ? 4 : 2;
+            float S[NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) yacc[r][n][e] = 0.0f;
-
-        // MMA: B fragments of the warp's group for the current step, and the
-        // next step's prefetched while the current one computes (bf16/f16
-        // activations; the f32 hi/lo split loads at step start).
-        constexpr bool PREFETCH = (MODE == PATH_MMA) && !XSPLIT;
-        uint32_t bcur[NT][8][2], bnxt[PREFETCH ? NT : 1][8][2];
-        uint32_t blo[XSPLIT ? NT : 1][8][2];
-        auto load_b = [&](int gg, uint32_t (&bh)[NT][8][2], uint32_t (&bl)[XSPLIT ? NT : 1][8][2]) {
-            const bool act = gg < un.g_end;
+                for (int e = 0; e < 4; ++e) S[n][e] = 0.0f;
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int m = 8 * n + gq;
+            for (int r0 = 0; r0 < RB; r0 += TI) {
+                uint32_t wv[TI][8];
+                float2 sp[TI];
+                uint32_t zp[TI];
+#pragma unroll
+                for (int i = 0; i < TI; ++i) {
+                    const uint8_t *tile = wtiles + (r0 + i) * W * TILE_BYTES;
+                    const bool live = r0 + i < nrt;
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
+                    sp[i] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
+                    zp[i] = *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq);
+                    wv[i][0] = c0.x; wv[i][1] = c0.y; wv[i][2] = c0.z; wv[i][3] = c0.w;
+                    wv[i][4] = c1.x; wv[i][5] = c1.y; wv[i][6] = c1.z; wv[i][7] = c1.w;
+                }
+                float d[TI][NT][4];
+#pragma unroll
+                for (int i = 0; i < TI; ++i)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) d[i][n][e] = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int64_t k = static_cast<int64_t>(gg) * G + 16 * j + 2 * t;
+                    if (r0 == 0) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t vh = 0, vl = 0;
-                        if (act && m < M) {
-                            const int64_t idx = static_cast<int64_t>(m) * a.K + k + 8 * h;
-                            if (XSPLIT) {
-                                const float2 xv = __ldg(reinterpret_cast<const float2 *>(
-                                    static_cast<const float *>(a.x) + idx));
-                                vh = pack_bf16x2(xv.x, xv.y);
-                                vl = pack_bf16x2(xv.x - bf16_lo_f32(vh), xv.y - bf16_hi_f32(vh));
-                            } else {
-                                vh = __ldg(reinterpret_cast<const unsigned int *>(
-                                    static_cast<const uint16_t *>(a.x) + idx));
-                            }
+                        for (int n = 0; n < NT; ++n) {
+                            mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, bcur[n][j][0], bcur[n][j][1]);
+                            if (XSPLIT)
+                                mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, blo[XSPLIT ? n : 0][j][0],
+                                            blo[XSPLIT ? n : 0][j][1]);
                         }
-                        bh[n][j][h] = vh;
-                        if (XSPLIT) bl[XSPLIT ? n : 0][j][h] = vl;
                     }
-                }
-            }
-        };
-        if (MODE == PATH_MMA) load_b(un.g_begin + warp, bcur, blo);
-
-        for (int s = 0; s < un.nsteps; ++s, ++gstep) {
-            const int slot = gstep % NSTAGE;
-            const int g = un.g_begin + s * W + warp;
-            const bool active = g < un.g_end;
-
-            ok = mbar_wait_bounded(&full[slot], (gstep / NSTAGE) & 1, abort_flag, a.wait_ns, a.err);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            if (MODE == PATH_MMA && XSPLIT && s > 0) load_b(g, bcur, blo);
-            if (PREFETCH && s + 1 < un.nsteps)
-                load_b(g + W, reinterpret_cast<uint32_t (&)[NT][8][2]>(bnxt), blo);
-            const uint8_t *stage = ring + slot * STAGE_BYTES + warp * TILE_BYTES;
-            if (active && MODE == PATH_FMA) {
-                const int gl = g - un.g_begin;
-                const float4 *xpp =
-                    reinterpret_cast<const float4 *>(pairs + (gl * 4 + t) * PAIR_STRIDE);
-                float2 P[8][4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 p = xpp[2 * j], q = xpp[2 * j + 1];
-                    P[j][0] = make_float2(p.x, p.y);
-                    P[j][1] = make_float2(p.z, p.w);
-                    P[j][2] = make_float2(q.x, q.y);
-                    P[j][3] = make_float2(q.z, q.w);
-                }
-                const float4 xsv = reinterpret_cast<const float4 *>(pairs + FMA_PAIR_FLOATS)[gl * 4 + t];
-                // all RB tiles at once: RB independent accumulator chains
-                uint32_t wv[RB][8];
-                float2 sp[RB];
-                uint32_t zp[RB];
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    const uint8_t *tile = stage + r * W * TILE_BYTES;
-                    const bool live = r < un.nrt;
-                    const uint4 c0 = live ? *reinterpret_cast<const uint4 *>(tile + 16 * lane)
-                                          : make_uint4(0, 0, 0, 0);
-                    const uint4 c1 = live ? *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane)
-                                          : make_uint4(0, 0, 0, 0);
-                    sp[r] = live ? *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq)
-                                 : make_float2(0.0f, 0.0f);
-                    zp[r] = live ? *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq) : 0u;
-                    wv[r][0] = c0.x; wv[r][1] = c0.y; wv[r][2] = c0.z; wv[r][3] = c0.w;
-                    wv[r][4] = c1.x; wv[r][5] = c1.y; wv[r][6] = c1.z; wv[r][7] = c1.w;
-                }
-                float2 accG[RB], accG8[RB];
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    accG[r] = make_float2(0.0f, 0.0f);
-                    accG8[r] = make_float2(0.0f, 0.0f);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-#pragma unroll
-                    for (int r = 0; r < RB; ++r) {
-                        const uint32_t wj = wv[r][j], wn = wv[r][(j & 4) | ((j + 1) & 3)];
-                        accG[r] = __ffma2_rn(code_pair(wj), P[j][0], accG[r]);
-                        accG8[r] = __ffma2_rn(code_pair(wj >> 8), P[j][1], accG8[r]);
-                        accG8[r] = __ffma2_rn(code_pair(wj << 8), P[j][2], accG8[r]);
-                        accG[r] = __ffma2_rn(code_pair(__funnelshift_r(wj, wn, 16)), P[j][3], accG[r]);
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    const float zg = static_cast<float>(zp[r] & 0xFFu);
-                    const float zg8 = static_cast<float>(zp[r] >> 8);
-                    const float ig =
-                        fmaf(128.0f, accG[r].x, fmaf(2048.0f, accG[r].y, -fmaf(zg, xsv.x, xsv.y)));
-                    const float ig8 =
-                        fmaf(128.0f, accG8[r].x, fmaf(2048.0f, accG8[r].y, -fmaf(zg8, xsv.x, xsv.z)));
-                    yacc[r][0][0] = fmaf(sp[r].x, ig, yacc[r][0][0]);
-                    yacc[r][0][2] = fmaf(sp[r].y, ig8, yacc[r][0][2]);
-                }
-            } else if (active && MODE == PATH_MMA) {
-                const uint32_t MAG = ABT == 0 ? 0x43004300u : 0x64006400u;
-                const uint32_t ONES = ABT == 0 ? 0x3F803F80u : 0x3C003C00u;
-                const float OFF = ABT == 0 ? 128.0f : 1024.0f;
-                // TI tiles at a time: TI * NT independent accumulator chains,
-                // plus NT chains for the activation sums
-                constexpr int TI = (NT == 1) ? 4 : 2;
-                float S[NT][4];
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) S[n][e] = 0.0f;
-#pragma unroll
-                for (int r0 = 0; r0 < RB; r0 += TI) {
-                    uint32_t wv[TI][8];
-                    float2 sp[TI];
-                    uint32_t zp[TI];
 #pragma unroll
                     for (int i = 0; i < TI; ++i) {
-                        const uint8_t *tile = stage + (r0 + i) * W * TILE_BYTES;
-                        const bool live = r0 + i < un.nrt;
-                        const uint4 c0 = live ? *reinterpret_cast<const uint4 *>(tile + 16 * lane)
-                                              : make_uint4(0, 0, 0, 0);
-                        const uint4 c1 = live ? *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane)
-                                              : make_uint4(0, 0, 0, 0);
-                        sp[i] = live ? *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq)
-                                     : make_float2(0.0f, 0.0f);
-                        zp[i] = live ? *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq) : 0u;
-                        wv[i][0] = c0.x; wv[i][1] = c0.y; wv[i][2] = c0.z; wv[i][3] = c0.w;
-                        wv[i][4] = c1.x; wv[i][5] = c1.y; wv[i][6] = c1.z; wv[i][7] = c1.w;
-                    }
-                    float d[TI][NT][4];
-#pragma unroll
-                    for (int i = 0; i < TI; ++i)
-#pragma unroll
-                        for (int n = 0; n < NT; ++n)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) d[i][n][e] = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (r0 == 0) {
-#pragma unroll
-                            for (int n = 0; n < NT; ++n) {
-                                mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, bcur[n][j][0], bcur[n][j][1]);
-                                if (XSPLIT)
-                                    mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, blo[XSPLIT ? n : 0][j][0],
-                                                blo[XSPLIT ? n : 0][j][1]);
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < TI; ++i) {
-                            const uint32_t w = wv[i][j];
+                        const uint32_t w = wv[i][j];
+                        if (NT == 1 && !XSPLIT) {
+                            mma_word<ABT>(d[i][0], w, bcur[0][j][0], bcur[0][j][1]);
+                        } else {
                             const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
                             const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
                             const uint32_t a3 = lop3_and_or(w >> 8, 0x000F000Fu, MAG);
@@ -497,36 +508,37 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                             }
                         }
                     }
+                }
 #pragma unroll
-                    for (int i = 0; i < TI; ++i) {
-                        const float zg = OFF + static_cast<float>(zp[i] & 0xFFu);
-                        const float zg8 = OFF + static_cast<float>(zp[i] >> 8);
+                for (int i = 0; i < TI; ++i) {
+                    const float zg = OFF + static_cast<float>(zp[i] & 0xFFu);
+                    const float zg8 = OFF + static_cast<float>(zp[i] >> 8);
 #pragma unroll
-                        for (int n = 0; n < NT; ++n) {
-                            float *ya = yacc[r0 + i][n];
-                            ya[0] = fmaf(sp[i].x, fmaf(-zg, S[n][0], d[i][n][0]), ya[0]);
-                            ya[1] = fmaf(sp[i].x, fmaf(-zg, S[n][1], d[i][n][1]), ya[1]);
-                            ya[2] = fmaf(sp[i].y, fmaf(-zg8, S[n][0], d[i][n][2]), ya[2]);
-                            ya[3] = fmaf(sp[i].y, fmaf(-zg8, S[n][1], d[i][n][3]), ya[3]);
-                        }
+                    for (int n = 0; n < NT; ++n) {
+                        float *ya = yacc[r0 + i][n];
+                        ya[0] = fmaf(sp[i].x, fmaf(-zg, S[n][0], d[i][n][0]), ya[0]);
+                        ya[1] = fmaf(sp[i].x, fmaf(-zg, S[n][1], d[i][n][1]), ya[1]);
+                        ya[2] = fmaf(sp[i].y, fmaf(-zg8, S[n][0], d[i][n][2]), ya[2]);
+                        ya[3] = fmaf(sp[i].y, fmaf(-zg8, S[n][1], d[i][n][3]), ya[3]);
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (PREFETCH) {
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        bcur[n][j][0] = bnxt[PREFETCH ? n : 0][j][0];
-                        bcur[n][j][1] = bnxt[PREFETCH ? n : 0][j][1];
-                    }
-            }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (PREFETCH) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    bcur[n][j][0] = bnxt[PREFETCH ? n : 0][j][0];
+                    bcur[n][j][1] = bnxt[PREFETCH ? n : 0][j][1];
+                }
+        }
 
-        // ------------------------------------------- reduction and output
+        if (!(it == end - 1 || s == NS - 1)) continue;
+
+        // ----------------------------- this CTA's share of row block rb is done
         if (MODE == PATH_FMA) {
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
@@ -554,31 +566,37 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         }
         named_barrier_sync(1, CONSUMERS);
 
-        const int nout = un.nrt * 16 * Mo;
-        const int row0 = un.rt0 * TILE_ROWS;
+        const int64_t first_item = static_cast<int64_t>(rb) * NS;
+        const int c_first = static_cast<int>(owner_of(first_item, T, Gc));
+        const int c_last = static_cast<int>(owner_of(first_item + NS - 1, T, Gc));
+        const int nc = c_last - c_first + 1;
+        const int nout = nrt * 16 * Mo;
+        const int row0 = rb * RB * TILE_ROWS;
+        const int64_t slab = static_cast<int64_t>(RB * 16) * M;  // one contributor's partial
+        float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
         for (int i = threadIdx.x; i < nout; i += CONSUMERS) {
             const int row = i / Mo, m = i % Mo;
             float v = 0.0f;
 #pragma unroll
             for (int w = 0; w < W; ++w) v += red[(w * RB * 16 + row) * MS + m];
-            if (a.ks == 1) {
+            if (nc == 1) {
                 if (row0 + row < a.N)
                     store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v);
             } else {
-                a.partial[(static_cast<int64_t>(un.ks) * M + m) * npad + row0 + row] = v;
+                part[(blockIdx.x - c_first) * slab + i] = v;
             }
         }
-        if (a.ks > 1) {
-            // Split over K: the last unit of this row block sums the slices in
-            // order.  One thread publishes the CTA's partials (the barrier
-            // orders the other threads' stores before its release fence) and
+        if (nc > 1) {
+            // The last contributor to arrive sums the partials in CTA order.
+            // One thread publishes this CTA's partials (the barrier orders
+            // the other threads' stores before its release fence) and
             // acquires the others' before the barrier that releases the reads.
             named_barrier_sync(1, CONSUMERS);
             if (threadIdx.x == 0) {
                 __threadfence();
-                const unsigned int prev = atomicAdd(&a.count[un.rb], 1u);
+                const unsigned int prev = atomicAdd(&a.count[rb], 1u);
                 __threadfence();
-                *last_flag = (prev == static_cast<unsigned int>(a.ks - 1));
+                *last_flag = (prev == static_cast<unsigned int>(nc - 1));
             }
             named_barrier_sync(1, CONSUMERS);
             if (*last_flag) {
@@ -586,14 +604,13 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                     const int row = i / Mo, m = i % Mo;
                     if (row0 + row >= a.N) continue;
                     float v = 0.0f;
-                    for (int s2 = 0; s2 < a.ks; ++s2)
-                        v += __ldcg(&a.partial[(static_cast<int64_t>(s2) * M + m) * npad + row0 + row]);
+                    for (int c = 0; c < nc; ++c) v += __ldcg(&part[c * slab + i]);
                     store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v);
                 }
-                if (threadIdx.x == 0) a.count[un.rb] = 0u;  // ready for the next call
+                if (threadIdx.x == 0) a.count[rb] = 0u;  // ready for the next call
             }
         }
-        // red, pairs and last_flag are reused by the next unit
+        // red and last_flag are reused by the next row block
         named_barrier_sync(1, CONSUMERS);
     }
 }
@@ -601,28 +618,38 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 // -------------------------------------------------------------------- host
 template <int MODE, int NT, int ABT, bool XSPLIT>
 struct Kern {
-    static cudaError_t configure(int dev, int *blocks_per_sm)
+    static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    static int smem(int M)
     {
-        static int cached[64] = {};
-        if (dev >= 0 && dev < 64 && cached[dev] > 0) {
-            *blocks_per_sm = cached[dev];
+        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : 8 * NT);
+    }
+    static cudaError_t configure(int dev, int M, int *blocks_per_sm)
+    {
+        static int cached[64][17] = {};
+        static bool attr[64] = {};
+        if (dev < 0 || dev >= 64 || M < 1 || M > 16) return cudaErrorInvalidValue;
+        if (cached[dev][M] > 0) {
+            *blocks_per_sm = cached[dev][M];
             return cudaSuccess;
         }
         auto kern = k_gemv<MODE, NT, ABT, XSPLIT>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes(MODE));
-        if (e != cudaSuccess) return e;
+        if (!attr[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 smem(16));
+            if (e != cudaSuccess) return e;
+            attr[dev] = true;
+        }
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, THREADS, smem_bytes(MODE));
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, THREADS, smem(M));
         if (e != cudaSuccess) return e;
         if (n < 1) n = 1;
-        if (dev >= 0 && dev < 64) cached[dev] = n;
+        cached[dev][M] = n;
         *blocks_per_sm = n;
         return cudaSuccess;
     }
     static cudaError_t launch(int grid, const GemvArgs &a, cudaStream_t s)
     {
-        k_gemv<MODE, NT, ABT, XSPLIT><<<grid, THREADS, smem_bytes(MODE), s>>>(a);
+        k_gemv<MODE, NT, ABT, XSPLIT><<<grid, THREADS, smem(a.M), s>>>(a);
         return cudaGetLastError();
     }
 };
@@ -645,40 +672,33 @@ size_t counters_bytes(int nrb)
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
 {
     GemvPlan p{};
-    if (path == PATH_AUTO) path = (M == 1) ? PATH_FMA : PATH_MMA;
+    // AUTO: the tensor-core path for bf16/f16 activations (its unpack costs 7
+    // ALU instructions per 8 weights against 11 for the CUDA-core path, which
+    // is bound by the ALU pipe near half of HBM bandwidth); the CUDA-core path
+    // for f32 activations at M = 1 (the tensor-core path would need two MMAs
+    // per step for the hi/lo split of each activation).
+    if (path == PATH_AUTO) path = (M == 1 && xt == Q4_F32) ? PATH_FMA : PATH_MMA;
     p.path = path;
     p.rb = RB;
     const int ntiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int NG = K / G;
+    const int NS = (NG + W - 1) / W;
     p.nrb = (ntiles + RB - 1) / RB;
     int dev = 0, per_sm = 1;
     cudaGetDevice(&dev);
-    dispatch(path, M, xt, [&](auto k) { return decltype(k)::configure(dev, &per_sm); });
-    const long slots = static_cast<long>(sm_count) * per_sm;
-    const int gs_max = (path == PATH_FMA) ? GS_MAX_FMA : GS_MAX_MMA;
-    // Pick the K slice: units per CTA slot rounded up (the static round-robin
-    // tail) times the work per unit (steps of W groups plus about one step of
-    // per-unit overhead), plus the split-K partial traffic in step units.
-    double best = -1.0;
-    int best_gs = NG < gs_max ? NG : gs_max;
-    for (int gs = (NG < gs_max ? NG : gs_max); gs >= 1; --gs) {
-        const int ks = (NG + gs - 1) / gs;
-        if ((ks - 1) * gs >= NG) continue;
-        const long units = static_cast<long>(p.nrb) * ks;
-        const long per_cta = (units + slots - 1) / slots;
-        const double steps = (gs + W - 1) / W + 1.0 + (ks > 1 ? 0.5 : 0.0);
-        const double partial = ks > 1 ? 8.0 * ks * M / (0.539 * K) * (NG / 4.0) : 0.0;
-        const double cost = static_cast<double>(per_cta) * steps * slots / p.nrb + partial;
-        if (best < 0 || cost < best - 1e-9) {
-            best = cost;
-            best_gs = gs;
-        }
+    dispatch(path, M, xt, [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    const int64_t T = static_cast<int64_t>(p.nrb) * NS;
+    const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+    p.grid = static_cast<int>(T < slots ? T : slots);
+    // most CTAs sharing one row block
+    int maxc = 1;
+    for (int64_t rb = 0; rb < p.nrb; ++rb) {
+        const int64_t c0 = owner_of(rb * NS, T, p.grid), c1 = owner_of(rb * NS + NS - 1, T, p.grid);
+        if (c1 - c0 + 1 > maxc) maxc = static_cast<int>(c1 - c0 + 1);
     }
-    p.gs = best_gs;
-    p.ks = (NG + best_gs - 1) / best_gs;
-    p.grid = static_cast<int>(std::min<long>(static_cast<long>(p.nrb) * p.ks, slots));
-    p.workspace = p.ks > 1 ? counters_bytes(p.nrb) + static_cast<size_t>(p.ks) * M * ntiles *
-                                                         TILE_ROWS * sizeof(float)
+    p.maxc = maxc;
+    p.workspace = maxc > 1 ? counters_bytes(p.nrb) + static_cast<size_t>(p.nrb) * maxc * RB * 16 *
+                                                         static_cast<size_t>(M) * sizeof(float)
                            : 0;
     return p;
 }
