@@ -175,6 +175,27 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
 q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                   void *y, q4_dtype yt, q4_stream_t stream);
 
+/* Size of the static scratch array used by q4_gemv_noalloc (16 MiB; held on
+ * every GPU that loads this library until the process exits). */
+#define Q4_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * q4_gemv without a workspace argument, for callers that cannot allocate
+ * device memory (a plugin whose host framework owns all device memory and
+ * passes only inputs and outputs; a decode loop that must never call an
+ * allocator; a process whose GPU memory is reserved by another allocator).
+ * No counterpart on the pages: it exists only for those callers.
+ * Same arguments and results as q4_gemv (same kernels).  The workspace comes
+ * from a static device array of Q4_NOALLOC_SCRATCH_BYTES; problems that need
+ * more return Q4_ERR_UNSUPPORTED before any launch.  Allocates nothing.  The
+ * first call on each device looks up the array's address with that device
+ * current (make it before any stream capture).  All calls on a device share
+ * the array and each clears its counter block with an asynchronous memset on
+ * `stream`; calls that overlap on the GPU race, so order them.
+ */
+q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream);
+
 /* Synchronises `stream` and reports errors raised on the device since the
  * last check: Q4_ERR_TIMEOUT when a bounded wait inside a kernel gave up
  * (the kernel then returned without writing its outputs), Q4_ERR_CUDA for a

@@ -26,6 +26,7 @@ SOURCES = {
     "quantize.cu": ["--fmad=false", "-prec-div=true", "-ftz=false"],
     "gemv.cu": [],
     "gemm_tc.cu": [],
+    "noalloc.cu": [],
 }
 
 

@@ -1,0 +1,83 @@
+// noalloc.cu -- q4_gemv_noalloc: the decode GEMV for callers that cannot
+// allocate device memory.
+//
+// q4_gemv needs a caller-provided workspace when a row block's K range is
+// shared by several CTAs (arrival counters + partial sums).  Some callers
+// cannot provide one: a plugin or operator running inside a host framework
+// that owns all device memory and hands over only its input and output
+// buffers, a latency-critical decode loop that must never call into an
+// allocator (cudaMalloc can block on device-wide synchronisation and can fail
+// once a caching allocator has reserved the GPU), or a process whose device
+// memory is fully reserved by another allocator.  This entry point uses a
+// fixed scratch array in the library's own static device memory instead.
+//
+// Costs and rules of that choice:
+//   * every GPU that loads this library holds Q4_NOALLOC_SCRATCH_BYTES of it
+//     until the process exits;
+//   * problems whose workspace would exceed that size are rejected with
+//     Q4_ERR_UNSUPPORTED before anything is launched;
+//   * all calls on a device share the one array, which keeps the last call's
+//     contents: each call clears the counter block it relies on (an
+//     asynchronous memset on the same stream, no allocation), and calls that
+//     overlap on the GPU (e.g. concurrent streams) race on the array, so
+//     callers must order them;
+//   * the first call on each device looks up the array's device address
+//     (cudaGetSymbolAddress, with that device current) and caches it; make
+//     that first call before starting any stream capture.
+// Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_q4_scratch[Q4_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {};
+
+// Device address of the scratch array on the current device (looked up once
+// per device); nullptr with *err set on failure.
+void *scratch_for_current_device(cudaError_t *err)
+{
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_q4_scratch);
+        if (*err != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                                     const void *qw, void *y, q4_dtype yt, q4_stream_t stream)
+{
+    if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
+    if (N < 1 || K < Q4_GROUP || K % Q4_GROUP != 0) return Q4_ERR_INVALID_ARG;
+    if (M < 1 || M > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED;
+    const size_t need = q4_gemv_workspace_bytes(M, N, K);
+    if (need > Q4_NOALLOC_SCRATCH_BYTES) return Q4_ERR_UNSUPPORTED;  // beyond the static maximum
+    cudaError_t err = cudaSuccess;
+    void *scratch = scratch_for_current_device(&err);
+    if (!scratch) return Q4_ERR_CUDA;
+    if (need > 0) {
+        // The arrival counters (one u32 per 64 output rows, padded to 256
+        // bytes, at the start of the workspace) must start at zero.
+        const size_t rows64 = static_cast<size_t>((N + 63) / 64);
+        const size_t counters = ((rows64 * sizeof(unsigned int) + 255) / 256) * 256;
+        err = cudaMemsetAsync(scratch, 0, counters < need ? counters : need,
+                              reinterpret_cast<cudaStream_t>(stream));
+        if (err != cudaSuccess) return Q4_ERR_CUDA;
+    }
+    return q4_gemv(x, xt, M, N, K, qw, y, yt, need > 0 ? scratch : nullptr, need, stream);
+}
