@@ -169,8 +169,12 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
  * layout": dequantize in shared memory and feed the tensor cores in the same
  * pass).  W_hat is formed tile by tile in shared memory as bf16 (or f16 for
  * f16 activations) and multiplied on the tcgen05 tensor cores with f32
- * accumulators in tensor memory.  x: [M][K] BF16 or F16; y: [M][N] of yt.
- * Requires M >= 1, N % 16 == 0; x, qw and y 16-byte aligned.
+ * accumulators in tensor memory.  x: [M][K] BF16 or F16; y: [M][N] BF16 or
+ * F16 (f32 is UNSUPPORTED here).  Requires M >= 1, N % 16 == 0; x, qw and y
+ * 16-byte aligned.  Each w_hat is rounded once to the activation type, so the
+ * product differs from the exact dequantized product by at most one rounding
+ * of each w_hat (2^-9 relative for bf16) -- statistically far below
+ * 1e-3 * sum|w_hat x| for non-adversarial data.
  */
 q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                   void *y, q4_dtype yt, q4_stream_t stream);

@@ -195,6 +195,24 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
                        reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 1, 20000000ull);
 }
 
+q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                  void *y, q4_dtype yt, q4_stream_t stream)
+{
+    if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
+    if (M < 1 || M > (1LL << 30) || !sizes_ok(N, K) || N % 16 != 0 || N > (1LL << 30))
+        return Q4_ERR_INVALID_ARG;
+    if ((xt != Q4_BF16 && xt != Q4_F16) || (yt != Q4_BF16 && yt != Q4_F16))
+        return Q4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(y)) return Q4_ERR_MISALIGNED;
+    const DevInfo *d = dev_info();
+    if (!d) return cuda_fail(cudaGetLastError());
+    cudaError_t e = cudaSuccess;
+    const q4_status st = gemm_run(x, xt, M, N, K, qw, y, yt, d->sm_count, d->err,
+                                  reinterpret_cast<cudaStream_t>(stream), &e);
+    if (st == Q4_ERR_CUDA) return cuda_fail(e);
+    return st;
+}
+
 q4_status q4_check(q4_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -125,6 +125,18 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching (its CTAs become resident as ours exit), and wait until the
+// previous kernel on the stream has completed and its writes are visible.
+__device__ __forceinline__ void grid_dep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // d = (a & b) | c  as one LOP3
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c)
 {
@@ -181,6 +193,9 @@ cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8
                           int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
 cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
                           uint8_t *zero, cudaStream_t s);
+q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                   void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
+                   cudaError_t *cerr);
 cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
                         cudaStream_t s);
 

@@ -1,9 +1,522 @@
-// gemm_tc.cu -- large-M W4A16 GEMM on the tcgen05 tensor cores (in progress).
+// gemm_tc.cu -- large-M W4A16 GEMM on the sm_103a tcgen05 tensor cores.
+//
+// Y[M][N] = X[M][K] * W_hat[N][K]^T with W_hat = (q - zero) * scale per group
+// of 128 along K (page "Weight quantization", "How it works"), the weights
+// dequantized tile by tile in shared memory and fed to the tensor cores in the
+// same pass (page "LLM Quantization Architecture in Depth", "Kernels and
+// memory layout"); the fp weights never reach HBM.
+//
+// One persistent CTA per SM, 10 warps with fixed roles:
+//   warp 0     producer: activation tiles by 2-D tensor TMA (128-byte
+//              swizzle) and packed weight tiles by 1-D bulk copies;
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma;
+//   warps 2-5  dequantize: codes -> bf16 (or f16) w_hat = (q - zero) * scale,
+//              written in the K-major 128-byte-swizzled layout the MMA reads;
+//   warps 6-9  epilogue: tcgen05.ld of the accumulators -> bf16/f16 ->
+//              swizzled staging -> 2-D tensor TMA store.
+// CTA tile: 256 rows of X (two M=128 MMAs sharing one dequantized weight tile,
+// so each weight tile is dequantized once per 256 tokens) x 128 weight rows,
+// K in stages of 64.  Accumulators: 2 x 128 x 128 f32 per tile in tensor
+// memory, double-buffered (512 columns) so the epilogue of one tile overlaps
+// the MMAs of the next.  Every barrier wait is bounded; on expiry the CTA
+// raises the device error word, stops, drains its copies and MMAs, frees its
+// tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
-extern "C" q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                             const void *qw, void *y, q4_dtype yt, q4_stream_t stream)
+namespace q4 {
+namespace gm {
+
+constexpr int BM = 256, SUB = 128, BN = 128, BK = 64;
+constexpr int NA = 3;   // activation stages
+constexpr int NBS = 3;  // dequantized-weight stages
+constexpr int NC = 2;   // packed-code stages (one group = two k stages)
+constexpr int RT = BN / TILE_ROWS;         // 8 row tiles per weight tile
+constexpr int A_BOX = SUB * BK * 2;        // 16384: one 128 x 64 activation box
+constexpr int A_STAGE = 2 * A_BOX;         // 32768
+constexpr int B_STAGE = BN * BK * 2;       // 16384
+constexpr int C_STAGE = RT * TILE_BYTES;   // 8832
+constexpr int E_BOX = 32 * 128;            // 32 rows x 128 bytes of output
+constexpr int E_WARP = 2 * E_BOX;          // 64 output columns x 2 boxes = 128 columns
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NA * A_STAGE;
+constexpr int OFF_C = OFF_B + NBS * B_STAGE;
+constexpr int OFF_E = ((OFF_C + NC * C_STAGE + 1023) / 1024) * 1024;
+constexpr int OFF_BAR = OFF_E + 4 * E_WARP;
+constexpr int SMEM_USED = OFF_BAR + 256;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+constexpr int THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+
+static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_E % 1024 == 0, "alignment");
+static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
+
+// ----------------------------------------------------------------- PTX
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar)
 {
-    (void)x; (void)xt; (void)M; (void)N; (void)K; (void)qw; (void)y; (void)yt; (void)stream;
-    return Q4_ERR_UNSUPPORTED;
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
 }
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (tcgen05 descriptor format, version 1).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;    // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= static_cast<uint64_t>(1) << 46;           // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulate, A/B bf16 (ab = 1) or
+// f16 (ab = 0), both K-major, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab)
+{
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two codes of a bf16 pair (128 + q_a | 128 + q_b) -> (q - zero) * scale,
+// rounded once from f32 to bf16/f16, packed (a in the low half).
+template <bool F16>
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t p, float neg_z, float s)
+{
+    float2 v = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+    v = __fadd2_rn(v, make_float2(neg_z, neg_z));  // exact: small integers
+    v = __fmul2_rn(v, make_float2(s, s));
+    if (F16) {
+        const __half2 h = __float22half2_rn(v);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 b = __float22bfloat162_rn(v);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+struct Args {
+    const uint8_t *qw;
+    int M, N, K;
+    int mt, nt;  // tiles along M (256 rows) and N (128 rows)
+    uint64_t wait_ns;
+    unsigned int *err;
+};
+
+// F16: activations (and the dequantized weights) are f16, else bf16.
+// YF16: outputs are f16, else bf16.
+template <bool F16, bool YF16>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+           const Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem + OFF_A;
+    uint8_t *sB = smem + OFF_B;
+    uint8_t *sC = smem + OFF_C;
+    uint8_t *sE = smem + OFF_E;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *full_a = bar, *empty_a = bar + NA;
+    uint64_t *full_b = bar + 2 * NA, *empty_b = full_b + NBS;
+    uint64_t *full_c = empty_b + NBS, *empty_c = full_c + NC;
+    uint64_t *acc_full = empty_c + NC, *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NG = a.K / G;
+    const int KS = a.K / BK;
+    const int ntiles_rows = (a.N + TILE_ROWS - 1) / TILE_ROWS;
+    const int T = a.mt * a.nt;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&full_a[i], 1);
+            mbar_init(&empty_a[i], 1);
+        }
+        for (int i = 0; i < NBS; ++i) {
+            mbar_init(&full_b[i], 4);
+            mbar_init(&empty_b[i], 1);
+        }
+        for (int i = 0; i < NC; ++i) {
+            mbar_init(&full_c[i], 1);
+            mbar_init(&empty_c[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            int ia = 0, ic = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
+                const int m0 = (tile % a.mt) * BM, nb = tile / a.mt;
+                const int rt0 = nb * RT, nrt = min(RT, ntiles_rows - rt0);
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int sa = ia % NA;
+                    if (ia >= NA && !mbar_wait_bounded(&empty_a[sa], ((ia / NA) - 1) & 1, abort_flag,
+                                                       a.wait_ns, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_a[sa], A_STAGE);
+                    tma_load_2d(sA + sa * A_STAGE, &tmx, ks * BK, m0, &full_a[sa]);
+                    tma_load_2d(sA + sa * A_STAGE + A_BOX, &tmx, ks * BK, m0 + SUB, &full_a[sa]);
+                    ++ia;
+                    if ((ks & 1) == 0) {
+                        const int sc = ic % NC;
+                        if (ic >= NC && !mbar_wait_bounded(&empty_c[sc], ((ic / NC) - 1) & 1,
+                                                           abort_flag, a.wait_ns, a.err)) {
+                            ok = false;
+                            break;
+                        }
+                        const int g = ks >> 1;
+                        mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TILE_BYTES);
+                        for (int r = 0; r < nrt; ++r)
+                            bulk_g2s(sC + sc * C_STAGE + r * TILE_BYTES,
+                                     a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TILE_BYTES,
+                                     TILE_BYTES, &full_c[sc]);
+                        ++ic;
+                    }
+                }
+            }
+            // every issued copy lands before the CTA may exit
+            for (int i = max(0, ia - NA); i < ia; ++i)
+                mbar_wait_bounded(&full_a[i % NA], (i / NA) & 1, abort_flag, a.wait_ns, a.err, false);
+            for (int i = max(0, ic - NC); i < ic; ++i)
+                mbar_wait_bounded(&full_c[i % NC], (i / NC) & 1, abort_flag, a.wait_ns, a.err, false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(F16 ? 0u : 1u);
+            int ia = 0, ib = 0, tt = 0;
+            bool issued = false, ok = true;
+            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
+                const int buf = tt & 1;
+                if (tt >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((tt >> 1) - 1) & 1, abort_flag,
+                                                  a.wait_ns, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int sa = ia % NA, sb = ib % NBS;
+                    if (!mbar_wait_bounded(&full_a[sa], (ia / NA) & 1, abort_flag, a.wait_ns, a.err) ||
+                        !mbar_wait_bounded(&full_b[sb], (ib / NBS) & 1, abort_flag, a.wait_ns, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + sa * A_STAGE), a1 = a0 + A_BOX;
+                    const uint32_t b0 = smem_u32(sB + sb * B_STAGE);
+#pragma unroll
+                    for (int k16 = 0; k16 < BK / 16; ++k16) {
+                        const uint32_t acc = (ks > 0 || k16 > 0) ? 1u : 0u;
+                        const uint64_t bd = sw128_desc(b0 + 32 * k16);
+                        mma_f16(d0, sw128_desc(a0 + 32 * k16), bd, idesc, acc);
+                        mma_f16(d1, sw128_desc(a1 + 32 * k16), bd, idesc, acc);
+                    }
+                    issued = true;
+                    mma_commit(&empty_a[sa]);
+                    mma_commit(&empty_b[sb]);
+                    ++ia;
+                    ++ib;
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[buf]);
+            }
+            if (issued) {
+                // all issued MMAs complete before tensor memory is freed
+                mma_commit(drain);
+                mbar_wait_bounded(drain, 0, abort_flag, a.wait_ns, a.err, false);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------ dequantize
+        const int d = warp - 2, gq = lane >> 2, t = lane & 3;
+        int ib = 0, ic = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
+            const int nb = tile / a.mt;
+            const int nrt = min(RT, ntiles_rows - nb * RT);
+            for (int ks = 0; ks < KS; ++ks) {
+                const int h = ks & 1, sc = ic % NC, sb = ib % NBS;
+                if (h == 0)
+                    ok = mbar_wait_bounded(&full_c[sc], (ic / NC) & 1, abort_flag, a.wait_ns, a.err);
+                if (ok && ib >= NBS)
+                    ok = mbar_wait_bounded(&empty_b[sb], ((ib / NBS) - 1) & 1, abort_flag, a.wait_ns,
+                                           a.err);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *bst = sB + sb * B_STAGE;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = 2 * d + rr;
+                    if (r < nrt) {
+                        const uint8_t *ct = sC + sc * C_STAGE + r * TILE_BYTES;
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(ct + h * 512 + 16 * lane);
+                        const float2 sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
+                        const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
+                        const float nz0 = -(128.0f + static_cast<float>(zp & 0xFFu));
+                        const float nz8 = -(128.0f + static_cast<float>(zp >> 8));
+                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                        uint8_t *row0 = bst + (16 * r + gq) * 128 + 4 * t;
+                        uint8_t *row8 = row0 + 8 * 128;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t w = words[i];
+                            const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);
+                            const uint32_t p1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+                            const uint32_t p3 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+                            const uint32_t p2 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+                            const int c_lo = ((2 * i) ^ gq) * 16, c_hi = ((2 * i + 1) ^ gq) * 16;
+                            *reinterpret_cast<uint32_t *>(row0 + c_lo) = dequant_pair<F16>(p0, nz0, sp.x);
+                            *reinterpret_cast<uint32_t *>(row0 + c_hi) = dequant_pair<F16>(p2, nz0, sp.x);
+                            *reinterpret_cast<uint32_t *>(row8 + c_lo) = dequant_pair<F16>(p1, nz8, sp.y);
+                            *reinterpret_cast<uint32_t *>(row8 + c_hi) = dequant_pair<F16>(p3, nz8, sp.y);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_b[sb]);
+                ++ib;
+                if (h == 1) {
+                    if (lane == 0) mbar_arrive(&empty_c[sc]);
+                    ++ic;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int p = warp & 3;  // tensor-memory lane quarter this warp may read
+        uint8_t *stg = sE + (warp - 6) * E_WARP;
+        int tt = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
+            const int m0 = (tile % a.mt) * BM, n0 = (tile / a.mt) * BN;
+            const int buf = tt & 1;
+            ok = mbar_wait_bounded(&acc_full[buf], (tt >> 1) & 1, abort_flag, a.wait_ns, a.err);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+                // the previous store must have finished reading the staging buffer
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * p) << 16) + buf * 256 + sub * 128 + 32 * c, v);
+                    uint32_t o[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 f = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        if (YF16) {
+                            const __half2 hh = __float22half2_rn(f);
+                            o[i] = *reinterpret_cast<const uint32_t *>(&hh);
+                        } else {
+                            const __nv_bfloat162 bb = __float22bfloat162_rn(f);
+                            o[i] = *reinterpret_cast<const uint32_t *>(&bb);
+                        }
+                    }
+                    // columns 32c..32c+31 of this lane's row: box c/2, chunks 4(c%2)..+3
+                    uint8_t *rowp = stg + (c >> 1) * E_BOX + lane * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = (4 * (c & 1) + q) ^ (lane & 7);
+                        *reinterpret_cast<uint4 *>(rowp + chunk * 16) =
+                            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int row = m0 + sub * SUB + 32 * p;
+                    if (row < a.M) {
+                        tma_store_2d(&tmy, n0, row, stg);
+                        if (n0 + 64 < a.N) tma_store_2d(&tmy, n0 + 64, row, stg + E_BOX);
+                    }
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (lane == 0) bulk_wait0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ----------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+static bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, uint64_t inner,
+                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gm
+
+q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                   void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
+                   cudaError_t *cerr)
+{
+    using namespace gm;
+    *cerr = cudaSuccess;
+    const bool f16 = (xt == Q4_F16);
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tmx, tmy;
+    if (!make_map(&tmx, x, dt, K, M, K * 2, BK, SUB)) return Q4_ERR_UNSUPPORTED;
+    const CUtensorMapDataType dy = (yt == Q4_F16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map(&tmy, y, dy, N, M, N * 2, 64, 32)) return Q4_ERR_UNSUPPORTED;
+    Args a{};
+    a.qw = static_cast<const uint8_t *>(qw);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.mt = static_cast<int>((M + BM - 1) / BM);
+    a.nt = static_cast<int>((N + BN - 1) / BN);
+    a.wait_ns = 2000000000ull;
+    a.err = err;
+    const int tiles = a.mt * a.nt;
+    const int grid = tiles < sm_count ? tiles : sm_count;
+    const bool yf16 = (yt == Q4_F16);
+    auto kern = f16 ? (yf16 ? k_gemm<true, true> : k_gemm<true, false>)
+                    : (yf16 ? k_gemm<false, true> : k_gemm<false, false>);
+    const int variant = (f16 ? 2 : 0) + (yf16 ? 1 : 0);
+    static bool configured[4][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[variant][dev]) {
+        *cerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
+        configured[variant][dev] = true;
+    }
+    kern<<<grid, THREADS, SMEM_ALLOC, s>>>(tmx, tmy, a);
+    *cerr = cudaGetLastError();
+    return *cerr == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+}  // namespace q4

@@ -7,18 +7,23 @@
 // turned into floating point in registers and never written back to memory.
 //
 // Work decomposition (stream-K): the output rows are cut into row blocks of
-// RB = 4 tiles (64 rows); each row block is a sequence of NS = ceil(NG/4)
+// RB = 8 tiles (128 rows); each row block is a sequence of NS = ceil(NG/4)
 // steps, a step being 4 consecutive groups along K.  The nrb * NS items are
-// split into `grid` contiguous, equal ranges, one per persistent CTA (a few
+// split into `grid` contiguous, equal ranges, one per persistent CTA (two
 // CTAs per SM).  A CTA accumulates the steps of a row block in registers and
 // writes the row block out when it reaches its last step; a row block whose
 // steps are spread over several CTAs is finished by the last of them to
 // arrive, which sums the partial results in CTA order (so results do not
 // depend on timing).
 //
+// Consecutive GEMVs on a stream overlap (programmatic dependent launch): each
+// kernel lets the next launch at once, and the next one's producer requests
+// its first stages of weight tiles before waiting for the previous kernel to
+// complete; activations, outputs and the workspace are touched only after.
+//
 // CTA = 4 consumer warps + 1 producer warp.  The producer streams each step's
 // weight tiles (RB row tiles x 4 groups) with 1-D bulk asynchronous copies
-// (TMA engine) into a 3-stage shared-memory ring and runs ahead across row
+// (TMA engine) into a 2-stage shared-memory ring and runs ahead across row
 // blocks, so the memory pipeline never drains.  Consumer warp w takes group w
 // of every step.
 //
@@ -45,8 +50,8 @@
 namespace q4 {
 
 constexpr int W = 4;        // consumer warps = groups per step
-constexpr int RB = 4;       // row tiles per row block
-constexpr int NSTAGE = 3;   // ring depth
+constexpr int RB = 8;       // row tiles per row block
+constexpr int NSTAGE = 2;   // ring depth
 constexpr int THREADS = (W + 1) * 32;
 constexpr int CONSUMERS = W * 32;
 constexpr int TILES_BYTES = RB * W * TILE_BYTES;  // 17664
@@ -58,7 +63,7 @@ constexpr int CTRL_BYTES = 128;                   // barriers + flags
 constexpr int PAIR_STRIDE = 68;
 constexpr int WARP_PAIR_FLOATS = 4 * PAIR_STRIDE + 4 * 4;
 constexpr int RED_FLOATS_FMA = W * RB * 16;
-constexpr int MIN_BLOCKS = 3;  // CTAs per SM the shared memory budget is sized for
+constexpr int MIN_BLOCKS = 2;  // CTAs per SM the shared memory budget is sized for
 
 constexpr int XROW = W * G * 2 + 16;  // MMA staged activations: one padded row per batch row
 
@@ -75,8 +80,9 @@ __host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms)
            (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4);
 }
 
-static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "three FMA CTAs per SM");
-static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 1, 8) + 1024) <= 228 * 1024, "three MMA CTAs per SM");
+
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "two FMA CTAs per SM");
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 8, 8) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
 
 __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float v)
 {
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     int *last_flag = const_cast<int *>(abort_flag) + 1;
     float *after = reinterpret_cast<float *>(smem + NSTAGE * SB + CTRL_BYTES);
     float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
-    constexpr int MSR = (MODE == PATH_FMA) ? 1 : 8 * NT;  // red row stride
+    const int MSR = (MODE == PATH_FMA) ? 1 : a.M;  // red row stride
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
@@ -236,14 +242,38 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         fence_barrier_init();
     }
     __syncthreads();
+    // The next GEMV on the stream may begin launching; its CTAs take SMs as
+    // ours exit and start streaming their (static) weights early.
+    grid_dep_launch_dependents();
 
     // ------------------------------------------------------------ producer
     if (warp == W) {
         if (lane == 0) {
             int gstep = 0;
             if (!a.debug_no_copy) {
-                for (int64_t it = beg; it < end; ++it, ++gstep) {
-                    const int rb = static_cast<int>(it / NS), s = static_cast<int>(it % NS);
+                // Weight tiles never depend on the previous kernel, so the
+                // first NSTAGE stages' tiles are requested before waiting for
+                // it; their activation copies follow the wait.
+                auto issue_x = [&](int slot, int g0, int ng) {
+                    uint8_t *stage = ring + slot * SB;
+                    if (MODE == PATH_FMA)
+                        bulk_g2s(stage + TILES_BYTES,
+                                 static_cast<const uint8_t *>(a.x) + static_cast<int64_t>(g0) * G * xb,
+                                 static_cast<uint32_t>(ng) * G * xb, &full[slot]);
+                    for (int m = 0; m < xrows; ++m)
+                        bulk_g2s(stage + TILES_BYTES + m * XROW,
+                                 static_cast<const uint8_t *>(a.x) +
+                                     (static_cast<int64_t>(m) * a.K + static_cast<int64_t>(g0) * G) * 2,
+                                 static_cast<uint32_t>(ng) * G * 2, &full[slot]);
+                };
+                int pro_g0[NSTAGE], pro_ng[NSTAGE];
+                const int npro = static_cast<int>(end - beg < NSTAGE ? end - beg : NSTAGE);
+                int rb = static_cast<int>(beg / NS), s = static_cast<int>(beg % NS);
+                for (int64_t it = beg; it < end; ++it, ++gstep, ++s) {
+                    if (s == NS) {
+                        s = 0;
+                        ++rb;
+                    }
                     const int slot = gstep % NSTAGE;
                     if (gstep >= NSTAGE &&
                         !mbar_wait_bounded(&empty[slot], ((gstep / NSTAGE) - 1) & 1, abort_flag,
@@ -260,15 +290,16 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                         bulk_g2s(stage + r * W * TILE_BYTES,
                                  a.qw + (static_cast<int64_t>(rt0 + r) * NG + g0) * TILE_BYTES,
                                  row_bytes, &full[slot]);
-                    if (MODE == PATH_FMA)
-                        bulk_g2s(stage + TILES_BYTES,
-                                 static_cast<const uint8_t *>(a.x) + static_cast<int64_t>(g0) * G * xb,
-                                 xbytes, &full[slot]);
-                    for (int m = 0; m < xrows; ++m)
-                        bulk_g2s(stage + TILES_BYTES + m * XROW,
-                                 static_cast<const uint8_t *>(a.x) +
-                                     (static_cast<int64_t>(m) * a.K + static_cast<int64_t>(g0) * G) * 2,
-                                 static_cast<uint32_t>(ng) * G * 2, &full[slot]);
+                    if (gstep < npro) {
+                        pro_g0[gstep] = g0;
+                        pro_ng[gstep] = ng;
+                        if (gstep == npro - 1) {
+                            grid_dep_wait();
+                            for (int p = 0; p < npro; ++p) issue_x(p, pro_g0[p], pro_ng[p]);
+                        }
+                    } else {
+                        issue_x(slot, g0, ng);
+                    }
                 }
             }
             // Every issued copy must land before the CTA may exit.
@@ -280,6 +311,9 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     }
 
     // ------------------------------------------------------------ consumers
+    // Activations, outputs and the workspace may belong to the previous
+    // kernel on the stream: touch none of them before it has completed.
+    grid_dep_wait();
     const int gq = lane >> 2, t = lane & 3;
     const int M = a.M;
     const int MS = MSR;
@@ -325,8 +359,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     float yacc[RB][NT][4];
     int gstep = 0;
     bool ok = true;
+    int rb = static_cast<int>(beg / NS), s = static_cast<int>(beg % NS) - 1;
     for (int64_t it = beg; it < end; ++it, ++gstep) {
-        const int rb = static_cast<int>(it / NS), s = static_cast<int>(it % NS);
+        if (++s == NS) {
+            s = 0;
+            ++rb;
+        }
         const int slot = gstep % NSTAGE;
         const int g = s * W + warp;
         const bool active = g < NG;
@@ -347,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         }
         if (MODE == PATH_MMA && XSPLIT && it > beg) load_b(g, bcur, blo);
         if (PREFETCH && it + 1 < end)
-            load_b(static_cast<int>((it + 1) % NS) * W + warp,
+            load_b((s + 1 == NS ? 0 : s + 1) * W + warp,
                    reinterpret_cast<uint32_t (&)[NT][8][2]>(bnxt), blo);
         const uint8_t *stage = ring + slot * SB;
         const uint8_t *wtiles = stage + warp * TILE_BYTES;
@@ -561,7 +599,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                     for (int e = 0; e < 4; ++e) {
                         const int row = r * 16 + gq + ((e & 2) ? 8 : 0);
                         const int m = 8 * n + 2 * t + (e & 1);
-                        red[(warp * RB * 16 + row) * MS + m] = yacc[r][n][e];
+                        if (m < M) red[(warp * RB * 16 + row) * MS + m] = yacc[r][n][e];
                     }
         }
         named_barrier_sync(1, CONSUMERS);
@@ -621,7 +659,7 @@ struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     static int smem(int M)
     {
-        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : 8 * NT);
+        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
     {
@@ -649,8 +687,17 @@ struct Kern {
     }
     static cudaError_t launch(int grid, const GemvArgs &a, cudaStream_t s)
     {
-        k_gemv<MODE, NT, ABT, XSPLIT><<<grid, THREADS, smem(a.M), s>>>(a);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem(a.M);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT>, a);
     }
 };
 
