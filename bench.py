@@ -342,9 +342,12 @@ def main():
     ap.add_argument("--case", default=None,
                     help="NxK: time one GEMV shape alone (small-case mode for profilers)")
     ap.add_argument("--reps", type=int, default=3, help="launches in --case mode")
+    ap.add_argument("--gemm-case", default=None, help="MxNxK: time one q4_gemm shape alone")
     args = ap.parse_args()
     if args.case:
         return single_case(args)
+    if args.gemm_case:
+        return gemm_case(args)
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_setup()
@@ -532,6 +535,27 @@ def extra_rows(q4, torch, work, pk) -> dict:
         sweep[name] = res
     rows["mlp_sweep"] = sweep
 
+    # large-M GEMM (prefill): 4096 tokens x 8192 x 28672, tcgen05 tensor cores
+    Mg, Ng, Kg = 4096, 28672, 8192
+    qg = work.qw[0][2]  # first 28672 rows of a fused gate+up weight
+    qg = q4.QWeight(qg.data[:q4.weight_bytes(Ng, Kg)], Ng, Kg)
+    xg = torch.empty(Mg * Kg, dtype=torch.int16, device=dev)
+    synth.dev_normal_bf16(xg.data_ptr(), Mg * Kg, 777, 0, 1.0)
+    xg = xg.view(torch.bfloat16).view(Mg, Kg)
+    yg = torch.empty((Mg, Ng), dtype=torch.bfloat16, device=dev)
+
+    def grun():
+        q4.gemm(xg, qg, out=yg)
+    g = graph_of(torch, grun)
+    t = time_graph(torch, g, reps=10)
+    flops = 2.0 * Mg * Ng * Kg
+    rows["gemm_prefill"] = {"shape": f"M={Mg} N={Ng} K={Kg} bf16", "ms": round(t * 1e3, 3),
+                            "TFLOP/s": round(flops / t / 1e12, 1),
+                            "frac_of_bf16_peak": round(flops / t / 1e12 / pk["bf16_tflops"], 4),
+                            "peak": pk["bf16_tflops"], "peak_kind": "burst, of measured"}
+    del g, xg, yg
+    torch.cuda.empty_cache()
+
     # quantizer: HBM-bound, 4 B read + 0.539 B written per weight
     N, K = 57344, 8192
     import synth
@@ -594,6 +618,37 @@ def single_case(args) -> int:
     print(json.dumps({"case": f"{N}x{K}", "M": M, "path": args.path, "copies": copies,
                       "launches": copies + args.reps, "us_per_call": round(t * 1e6, 2),
                       "GB/s": round(nb / t / 1e9, 1)}), flush=True)
+    return 0
+
+
+def gemm_case(args) -> int:
+    """One q4_gemm shape (bf16), `reps` launches after one warm-up."""
+    import torch
+
+    import synth
+    import weight_only_int4_group_gb300 as q4
+    M, N, K = (int(v) for v in args.gemm_case.lower().split("x"))
+    dev = torch.device("cuda")
+    w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    synth.dev_normal_f32(w.data_ptr(), N * K, 600, 0, SIGMA)
+    qw = q4.QWeight.from_float(w)
+    del w
+    x = torch.empty(M * K, dtype=torch.int16, device=dev)
+    synth.dev_normal_bf16(x.data_ptr(), M * K, 601, 0, 1.0)
+    x = x.view(torch.bfloat16).view(M, K)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    q4.gemm(x, qw, out=y)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        q4.gemm(x, qw, out=y)
+    b.record()
+    b.synchronize()
+    assert q4.check() == q4.OK
+    t = a.elapsed_time(b) / 1e3 / args.reps
+    print(json.dumps({"gemm_case": f"{M}x{N}x{K}", "ms": round(t * 1e3, 3),
+                      "TFLOP/s": round(2.0 * M * N * K / t / 1e12, 1)}), flush=True)
     return 0
 
 
