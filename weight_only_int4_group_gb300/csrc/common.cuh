@@ -128,6 +128,33 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer, so a decision taken on it is uniform.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Arrival counter step with acquire-release semantics at GPU scope: orders
+// the caller's earlier writes (and those ordered before them by a barrier)
+// before the increment, and later reads after it.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int *p, unsigned int v)
+{
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // Programmatic dependent launch: let the next kernel on the stream start
 // launching (its CTAs become resident as ours exit), and wait until the
 // previous kernel on the stream has completed and its writes are visible.

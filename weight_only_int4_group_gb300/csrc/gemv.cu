@@ -21,11 +21,16 @@
 // its first stages of weight tiles before waiting for the previous kernel to
 // complete; activations, outputs and the workspace are touched only after.
 //
-// CTA = 4 consumer warps + 1 producer warp.  The producer streams each step's
-// weight tiles (RB row tiles x 4 groups) with 1-D bulk asynchronous copies
-// (TMA engine) into a 2-stage shared-memory ring and runs ahead across row
-// blocks, so the memory pipeline never drains.  Consumer warp w takes group w
-// of every step.
+// CTA = 4 consumer warps + 1 producer warp + 1 epilogue warp.  The producer
+// streams each step's weight tiles (RB row tiles x 4 groups) with 1-D bulk
+// asynchronous copies (TMA engine) into a 2-stage shared-memory ring and runs
+// ahead across row blocks, so the memory pipeline never drains.  Consumer
+// warp w takes group w of every step.  When the consumers finish their share
+// of a row block they sum it over the warps into a shared-memory hand-off
+// buffer and go straight on to the next step; the epilogue warp writes the
+// rows out (or the partial sums, then the arrival counter and, if it arrives
+// last, the final sum), so global-memory round trips never stall the
+// consumers.
 //
 // Two consumer variants:
 //   FMA (M = 1): CUDA-core path.  A 4-bit code q at bit offset 16 or 12 of a
@@ -52,7 +57,7 @@ namespace q4 {
 constexpr int W = 4;        // consumer warps = groups per step
 constexpr int RB = 8;       // row tiles per row block
 constexpr int NSTAGE = 2;   // ring depth
-constexpr int THREADS = (W + 1) * 32;
+constexpr int THREADS = (W + 2) * 32;  // consumers, producer, epilogue
 constexpr int CONSUMERS = W * 32;
 constexpr int TILES_BYTES = RB * W * TILE_BYTES;  // 17664
 constexpr int XSTAGE_BYTES = W * G * 4;           // FMA: the step's activations (f32 worst case)
@@ -77,12 +82,14 @@ __host__ __device__ constexpr int stage_bytes(int mode, int xrows)
 __host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms)
 {
     return NSTAGE * stage_bytes(mode, xrows) + CTRL_BYTES +
-           (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4);
+           (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4) +
+           RB * 16 * ms * 4;  // hand-off buffer of one row block
 }
 
 
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "two FMA CTAs per SM");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 8, 8) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 0, 16) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
 
 __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float v)
 {
@@ -215,11 +222,13 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * SB);
     uint64_t *empty = full + NSTAGE;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NSTAGE);
-    int *last_flag = const_cast<int *>(abort_flag) + 1;
+    uint64_t *ofull = empty + NSTAGE;  // hand-off buffer written by the consumers
+    uint64_t *ofree = ofull + 1;       // hand-off buffer drained by the epilogue warp
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ofree + 1);
     float *after = reinterpret_cast<float *>(smem + NSTAGE * SB + CTRL_BYTES);
     float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
     const int MSR = (MODE == PATH_FMA) ? 1 : a.M;  // red row stride
+    float *out = red + W * RB * 16 * MSR;          // [RB * 16 rows][M]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
@@ -237,8 +246,9 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], W);
         }
+        mbar_init(ofull, 1);
+        mbar_init(ofree, 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -310,9 +320,89 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         return;
     }
 
+    // ------------------------------------------------------------ epilogue
+    // One hand-off per row block this CTA touches, in order.  A row block
+    // held by this CTA alone is written out directly.  Otherwise the partial
+    // sums go to this CTA's slot of the workspace and the arrival counter is
+    // stepped; the contributor that arrives last sums the partials of all
+    // contributors in CTA order (the same order whoever arrives last) and
+    // resets the counter for the next call.
+    if (warp == W + 1) {
+        // outputs and the workspace may belong to the previous kernel
+        grid_dep_wait();
+        if (beg < end) {
+            const int Mo = (MODE == PATH_FMA) ? 1 : a.M;
+            const int64_t slab = static_cast<int64_t>(RB * 16) * a.M;  // one contributor's partial
+            const int rb_first = static_cast<int>(beg / NS), rb_last = static_cast<int>((end - 1) / NS);
+            for (int rb = rb_first, e = 0; rb <= rb_last; ++rb, ++e) {
+                const bool ok = mbar_wait_bounded(ofull, e & 1, abort_flag, a.wait_ns, a.err);
+                if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
+                const int64_t first_item = static_cast<int64_t>(rb) * NS;
+                const int c_first = static_cast<int>(owner_of(first_item, T, Gc));
+                const int c_last = static_cast<int>(owner_of(first_item + NS - 1, T, Gc));
+                const int nc = c_last - c_first + 1;
+                const int nout = min(RB, ntiles - rb * RB) * 16 * Mo;
+                const int row0 = rb * RB * TILE_ROWS;
+                if (nc == 1) {
+                    for (int i = lane; i < nout; i += 32) {
+                        const int row = i / Mo, m = i % Mo;
+                        if (row0 + row < a.N)
+                            store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
+                    }
+                } else {
+                    float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
+                    for (int i = lane; i < nout; i += 32)
+                        part[(blockIdx.x - c_first) * slab + i] = out[i];
+                    __syncwarp();
+                    unsigned int prev = 0;
+                    if (lane == 0) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    __syncwarp();
+                    if (prev == static_cast<unsigned int>(nc - 1)) {
+                        // last to arrive: every partial is visible.  Four
+                        // outputs x four contributors of loads in flight at
+                        // once; the sums still run in CTA order.
+                        for (int i0 = lane; i0 < nout; i0 += 4 * 32) {
+                            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            for (int c0 = 0; c0 < nc; c0 += 4) {
+                                float pv[4][4];
+#pragma unroll
+                                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int i = i0 + 32 * u;
+                                        pv[cc][u] = (c0 + cc < nc && i < nout)
+                                                        ? __ldcg(&part[(c0 + cc) * slab + i])
+                                                        : 0.0f;
+                                    }
+#pragma unroll
+                                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u)
+                                        if (c0 + cc < nc) v[u] += pv[cc][u];
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = i0 + 32 * u;
+                                if (i >= nout) continue;
+                                const int row = i / Mo, m = i % Mo;
+                                if (row0 + row < a.N)
+                                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v[u]);
+                            }
+                        }
+                        if (lane == 0) a.count[rb] = 0u;  // ready for the next call
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ofree);
+            }
+        }
+        return;
+    }
+
     // ------------------------------------------------------------ consumers
-    // Activations, outputs and the workspace may belong to the previous
-    // kernel on the stream: touch none of them before it has completed.
+    // Activations may belong to the previous kernel on the stream: touch
+    // them only after it has completed.
     grid_dep_wait();
     const int gq = lane >> 2, t = lane & 3;
     const int M = a.M;
@@ -357,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         load_b(static_cast<int>(beg % NS) * W + warp, bcur, blo);
 
     float yacc[RB][NT][4];
-    int gstep = 0;
+    int gstep = 0, nepi = 0;
     bool ok = true;
     int rb = static_cast<int>(beg / NS), s = static_cast<int>(beg % NS) - 1;
     for (int64_t it = beg; it < end; ++it, ++gstep) {
@@ -448,7 +538,6 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
                 const uint8_t *tile = wtiles + r * W * TILE_BYTES;
-                const bool live = r < nrt;
                 const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
                 const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
                 sp[r] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
@@ -501,7 +590,6 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 #pragma unroll
                 for (int i = 0; i < TI; ++i) {
                     const uint8_t *tile = wtiles + (r0 + i) * W * TILE_BYTES;
-                    const bool live = r0 + i < nrt;
                     const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
                     const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
                     sp[i] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
@@ -602,54 +690,28 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                         if (m < M) red[(warp * RB * 16 + row) * MS + m] = yacc[r][n][e];
                     }
         }
-        named_barrier_sync(1, CONSUMERS);
-
-        const int64_t first_item = static_cast<int64_t>(rb) * NS;
-        const int c_first = static_cast<int>(owner_of(first_item, T, Gc));
-        const int c_last = static_cast<int>(owner_of(first_item + NS - 1, T, Gc));
-        const int nc = c_last - c_first + 1;
-        const int nout = nrt * 16 * Mo;
-        const int row0 = rb * RB * TILE_ROWS;
-        const int64_t slab = static_cast<int64_t>(RB * 16) * M;  // one contributor's partial
-        float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
-        for (int i = threadIdx.x; i < nout; i += CONSUMERS) {
-            const int row = i / Mo, m = i % Mo;
-            float v = 0.0f;
+        // The hand-off buffer is free once the epilogue warp has finished
+        // the previous row block; the barrier makes the decision uniform.
+        const bool stuck = nepi > 0 && !mbar_wait_bounded(ofree, (nepi - 1) & 1, abort_flag,
+                                                          a.wait_ns, a.err);
+        if (named_barrier_or(1, CONSUMERS, stuck)) {
+            ok = false;
+            break;
+        }
+        {
+            const int nout = nrt * 16 * Mo;
+            for (int i = threadIdx.x; i < nout; i += CONSUMERS) {
+                const int row = i / Mo, m = i % Mo;
+                float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < W; ++w) v += red[(w * RB * 16 + row) * MS + m];
-            if (nc == 1) {
-                if (row0 + row < a.N)
-                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v);
-            } else {
-                part[(blockIdx.x - c_first) * slab + i] = v;
+                for (int w = 0; w < W; ++w) v += red[(w * RB * 16 + row) * MS + m];
+                out[i] = v;
             }
         }
-        if (nc > 1) {
-            // The last contributor to arrive sums the partials in CTA order.
-            // One thread publishes this CTA's partials (the barrier orders
-            // the other threads' stores before its release fence) and
-            // acquires the others' before the barrier that releases the reads.
-            named_barrier_sync(1, CONSUMERS);
-            if (threadIdx.x == 0) {
-                __threadfence();
-                const unsigned int prev = atomicAdd(&a.count[rb], 1u);
-                __threadfence();
-                *last_flag = (prev == static_cast<unsigned int>(nc - 1));
-            }
-            named_barrier_sync(1, CONSUMERS);
-            if (*last_flag) {
-                for (int i = threadIdx.x; i < nout; i += CONSUMERS) {
-                    const int row = i / Mo, m = i % Mo;
-                    if (row0 + row >= a.N) continue;
-                    float v = 0.0f;
-                    for (int c = 0; c < nc; ++c) v += __ldcg(&part[c * slab + i]);
-                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v);
-                }
-                if (threadIdx.x == 0) a.count[rb] = 0u;  // ready for the next call
-            }
-        }
-        // red and last_flag are reused by the next row block
+        // red is reused by the next row block; the arrival publishes out
         named_barrier_sync(1, CONSUMERS);
+        if (threadIdx.x == 0) mbar_arrive(ofull);
+        ++nepi;
     }
 }
 
