@@ -66,6 +66,28 @@ def test_gemv_outlier_channels():
     compare(y, y_ref, absdot, where="outliers")
 
 
+def test_gemv_long_runs_per_cta_full_output():
+    """M = 1 with many steps per CTA (4096 x 40960: 32 row blocks x 80 steps,
+    at least 8 per CTA on a 152-SM part), the case served by the deeper
+    copy ring; every output against the oracle, bf16 and f16 activations,
+    and bitwise repeatable."""
+    import weight_only_int4_group_gb300 as q4
+    N, K = 4096, 40960
+    W = synth.normal_rows(77, K, 0, N, 0.02)
+    qw = _qweight(W)
+    o = oracle.load()
+    p, s, z = o.quantize(W)
+    for xdt in (torch.bfloat16, torch.float16):
+        x, xf = x_for(xdt, 1, K, seed=78)
+        y_ref, absdot = o.dot_naive(xf, p, s, z, N, K, threads=8)
+        y1 = q4.gemv(x, qw, out_dtype=torch.float32)
+        y2 = q4.gemv(x, qw, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert q4.check() == q4.OK
+        assert torch.equal(y1, y2)
+        compare(y1, y_ref, absdot, where=f"long runs x={xdt}")
+
+
 def test_gemv_deterministic_and_workspace_restored():
     import weight_only_int4_group_gb300 as q4
     N, K, M = 1000, 8192, 4

@@ -210,6 +210,7 @@ struct GemvPlan {
     int nrb;   // row blocks
     int grid;  // persistent CTAs
     int maxc;  // most CTAs sharing one row block (1: no partial sums)
+    bool deep; // 3-stage ring (M = 1, 16-bit activations, many steps per CTA)
     size_t workspace;
 };
 

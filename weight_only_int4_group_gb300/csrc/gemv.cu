@@ -56,7 +56,7 @@ namespace q4 {
 
 constexpr int W = 4;        // consumer warps = groups per step
 constexpr int RB = 8;       // row tiles per row block
-constexpr int NSTAGE = 2;   // ring depth
+constexpr int NSTAGE = 2;   // ring depth (3 for the M = 1 tensor-core kernel on long runs)
 constexpr int THREADS = (W + 2) * 32;  // consumers, producer, epilogue
 constexpr int CONSUMERS = W * 32;
 constexpr int TILES_BYTES = RB * W * TILE_BYTES;  // 17664
@@ -79,9 +79,9 @@ __host__ __device__ constexpr int stage_bytes(int mode, int xrows)
                             : ((TILES_BYTES + xrows * XROW + 127) / 128) * 128;
 }
 
-__host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms)
+__host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms, int nstage = NSTAGE)
 {
-    return NSTAGE * stage_bytes(mode, xrows) + CTRL_BYTES +
+    return nstage * stage_bytes(mode, xrows) + CTRL_BYTES +
            (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4) +
            RB * 16 * ms * 4;  // hand-off buffer of one row block
 }
@@ -90,6 +90,8 @@ __host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms)
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "two FMA CTAs per SM");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 8, 8) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 0, 16) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
+static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 1, 1, 3) + 1024) <= 228 * 1024,
+              "two 3-stage M = 1 MMA CTAs per SM");
 
 __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float v)
 {
@@ -212,7 +214,7 @@ __host__ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64
 
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
 // XSPLIT: f32 activations carried as bf16 hi + bf16 lo (two MMAs per step).
-template <int MODE, int NT, int ABT, bool XSPLIT>
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
     constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
@@ -220,12 +222,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     const int SB = stage_bytes(MODE, xrows);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * SB);
-    uint64_t *empty = full + NSTAGE;
-    uint64_t *ofull = empty + NSTAGE;  // hand-off buffer written by the consumers
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTG * SB);
+    uint64_t *empty = full + NSTG;
+    uint64_t *ofull = empty + NSTG;  // hand-off buffer written by the consumers
     uint64_t *ofree = ofull + 1;       // hand-off buffer drained by the epilogue warp
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ofree + 1);
-    float *after = reinterpret_cast<float *>(smem + NSTAGE * SB + CTRL_BYTES);
+    float *after = reinterpret_cast<float *>(smem + NSTG * SB + CTRL_BYTES);
     float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
     const int MSR = (MODE == PATH_FMA) ? 1 : a.M;  // red row stride
     float *out = red + W * RB * 16 * MSR;          // [RB * 16 rows][M]
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     const int xb = (a.xt == Q4_F32) ? 4 : 2;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < NSTG; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], W);
         }
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             int gstep = 0;
             if (!a.debug_no_copy) {
                 // Weight tiles never depend on the previous kernel, so the
-                // first NSTAGE stages' tiles are requested before waiting for
+                // first NSTG stages' tiles are requested before waiting for
                 // it; their activation copies follow the wait.
                 auto issue_x = [&](int slot, int g0, int ng) {
                     uint8_t *stage = ring + slot * SB;
@@ -276,17 +278,17 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                      (static_cast<int64_t>(m) * a.K + static_cast<int64_t>(g0) * G) * 2,
                                  static_cast<uint32_t>(ng) * G * 2, &full[slot]);
                 };
-                int pro_g0[NSTAGE], pro_ng[NSTAGE];
-                const int npro = static_cast<int>(end - beg < NSTAGE ? end - beg : NSTAGE);
+                int pro_g0[NSTG], pro_ng[NSTG];
+                const int npro = static_cast<int>(end - beg < NSTG ? end - beg : NSTG);
                 int rb = static_cast<int>(beg / NS), s = static_cast<int>(beg % NS);
                 for (int64_t it = beg; it < end; ++it, ++gstep, ++s) {
                     if (s == NS) {
                         s = 0;
                         ++rb;
                     }
-                    const int slot = gstep % NSTAGE;
-                    if (gstep >= NSTAGE &&
-                        !mbar_wait_bounded(&empty[slot], ((gstep / NSTAGE) - 1) & 1, abort_flag,
+                    const int slot = gstep % NSTG;
+                    if (gstep >= NSTG &&
+                        !mbar_wait_bounded(&empty[slot], ((gstep / NSTG) - 1) & 1, abort_flag,
                                            a.wait_ns, a.err))
                         break;
                     const int rt0 = rb * RB, nrt = min(RB, ntiles - rt0);
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 }
             }
             // Every issued copy must land before the CTA may exit.
-            for (int s = max(0, gstep - NSTAGE); s < gstep; ++s)
-                mbar_wait_bounded(&full[s % NSTAGE], (s / NSTAGE) & 1, abort_flag, a.wait_ns,
+            for (int s = max(0, gstep - NSTG); s < gstep; ++s)
+                mbar_wait_bounded(&full[s % NSTG], (s / NSTG) & 1, abort_flag, a.wait_ns,
                                   a.err, false);
         }
         return;
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             s = 0;
             ++rb;
         }
-        const int slot = gstep % NSTAGE;
+        const int slot = gstep % NSTG;
         const int g = s * W + warp;
         const bool active = g < NG;
         const int nrt = min(RB, ntiles - rb * RB);
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                     for (int e = 0; e < 4; ++e) yacc[r][n][e] = 0.0f;
         }
 
-        ok = mbar_wait_bounded(&full[slot], (gstep / NSTAGE) & 1, abort_flag, a.wait_ns, a.err);
+        ok = mbar_wait_bounded(&full[slot], (gstep / NSTG) & 1, abort_flag, a.wait_ns, a.err);
         if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -716,12 +718,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 }
 
 // -------------------------------------------------------------------- host
-template <int MODE, int NT, int ABT, bool XSPLIT>
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE>
 struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     static int smem(int M)
     {
-        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M);
+        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
     {
@@ -732,10 +734,10 @@ struct Kern {
             *blocks_per_sm = cached[dev][M];
             return cudaSuccess;
         }
-        auto kern = k_gemv<MODE, NT, ABT, XSPLIT>;
+        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG>;
         if (!attr[dev]) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 smem(16));
+                                                 smem(NSTG == NSTAGE ? 16 : 1));
             if (e != cudaSuccess) return e;
             attr[dev] = true;
         }
@@ -759,17 +761,25 @@ struct Kern {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT>, a);
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG>, a);
     }
 };
 
 template <typename F>
-static cudaError_t dispatch(int path, int M, q4_dtype xt, F &&f)
+static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, F &&f)
 {
     if (path == PATH_FMA) return f(Kern<PATH_FMA, 1, 0, false>{});
+    // deep: M = 1 with 16-bit activations, where a 3-stage ring still fits
+    // two CTAs per SM
     const bool two = M > 8;
-    if (xt == Q4_F16) return two ? f(Kern<PATH_MMA, 2, 1, false>{}) : f(Kern<PATH_MMA, 1, 1, false>{});
-    if (xt == Q4_BF16) return two ? f(Kern<PATH_MMA, 2, 0, false>{}) : f(Kern<PATH_MMA, 1, 0, false>{});
+    if (xt == Q4_F16) {
+        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3>{});
+        return two ? f(Kern<PATH_MMA, 2, 1, false>{}) : f(Kern<PATH_MMA, 1, 1, false>{});
+    }
+    if (xt == Q4_BF16) {
+        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3>{});
+        return two ? f(Kern<PATH_MMA, 2, 0, false>{}) : f(Kern<PATH_MMA, 1, 0, false>{});
+    }
     return two ? f(Kern<PATH_MMA, 2, 0, true>{}) : f(Kern<PATH_MMA, 1, 0, true>{});
 }
 
@@ -795,10 +805,19 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     p.nrb = (ntiles + RB - 1) / RB;
     int dev = 0, per_sm = 1;
     cudaGetDevice(&dev);
-    dispatch(path, M, xt, [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    dispatch(path, M, xt, false, [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
     const int64_t T = static_cast<int64_t>(p.nrb) * NS;
     const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
     p.grid = static_cast<int>(T < slots ? T : slots);
+    // The 3-stage ring pays off once each CTA streams many steps; with only a
+    // few, the deeper first wave of requests delays every CTA's first step.
+    p.deep = path == PATH_MMA && M == 1 && xt != Q4_F32 && T >= 8 * static_cast<int64_t>(p.grid);
+    if (p.deep) {  // same CTAs per SM, or keep the 2-stage ring
+        int per_sm_deep = 0;
+        dispatch(path, M, xt, true,
+                 [&](auto k) { return decltype(k)::configure(dev, M, &per_sm_deep); });
+        p.deep = per_sm_deep == per_sm;
+    }
     // most CTAs sharing one row block
     int maxc = 1;
     for (int64_t rb = 0; rb < p.nrb; ++rb) {
@@ -814,7 +833,8 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
 
 cudaError_t gemv_launch(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
 {
-    return dispatch(p.path, a.M, a.xt, [&](auto k) { return decltype(k)::launch(p.grid, a, s); });
+    return dispatch(p.path, a.M, a.xt, p.deep,
+                    [&](auto k) { return decltype(k)::launch(p.grid, a, s); });
 }
 
 }  // namespace q4
