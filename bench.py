@@ -187,8 +187,12 @@ class Decode70B:
         synth.dev_normal_bf16(self.x.data_ptr(), xo, seed + 7777, 0, 1.0)
         self.x = self.x.view(torch.bfloat16)
         self.y = torch.empty(yo, dtype=torch.bfloat16, device=dev)
-        wsb = max(q4.gemv_workspace_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
-        self.ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+        # one workspace per output size N: calls with the same N may share one
+        # (their counter blocks coincide); different N may not
+        self.ws = {}
+        for N in sorted({N for _, N, _ in LAYER_SHAPES}):
+            wsb = max(q4.gemv_workspace_bytes(M, N2, K) for _, N2, K in LAYER_SHAPES if N2 == N)
+            self.ws[N] = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
         self.bytes_per_step = layers * sum(algo_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
         self.weights_bytes = layers * sum(q4.weight_bytes(N, K) for _, N, K in LAYER_SHAPES)
         self.launches_per_step = layers * len(LAYER_SHAPES)
@@ -198,7 +202,7 @@ class Decode70B:
         q4 = self.q4
         x = self.x[self.x_off[l][i]:self.x_off[l][i] + self.M * K].view(self.M, K)
         y = self.y[self.y_off[l][i]:self.y_off[l][i] + self.M * N].view(self.M, N)
-        q4.gemv(x, self.qw[l][i], out=y, ws=self.ws, path=path)
+        q4.gemv(x, self.qw[l][i], out=y, ws=self.ws[N], path=path)
 
     def step(self, path=0):
         for l in range(self.L):

@@ -120,8 +120,12 @@ q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
  * when no split over K is used).  Layout: split-K arrival counters (one u32
  * per 64 output rows, padded to 256 B) followed by f32 partial sums.  The
  * counter block must be zero before the first call (zero-fill the buffer
- * once after allocation); every completed call leaves it zero again.  Calls
- * that may run concurrently need separate workspaces. */
+ * once after allocation); every completed call leaves it zero again.  One
+ * workspace may serve successive calls with the same N (their counter
+ * blocks coincide, whatever M and K); a call with another N would find the
+ * previous call's partial sums where its counters belong, so give each N its
+ * own workspace (or zero it between them).  Calls that may run concurrently
+ * need separate workspaces. */
 size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*

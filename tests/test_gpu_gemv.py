@@ -105,6 +105,38 @@ def test_gemv_deterministic_and_workspace_restored():
         assert int(cnt.abs().sum()) == 0
 
 
+def test_gemv_workspace_shared_by_calls_with_the_same_n():
+    """A decode layer's pattern: per-N workspaces, each shared by the shapes
+    with that N (8192 x 8192 and 8192 x 28672 share one), calls interleaved
+    and repeated; every output equals a call with a fresh workspace and the
+    counter blocks end at zero."""
+    import weight_only_int4_group_gb300 as q4
+    shapes = [(10240, 8192), (8192, 8192), (28672, 8192), (8192, 28672)]
+    qws, xs, refs = [], [], []
+    for i, (N, K) in enumerate(shapes):
+        w = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        synth.dev_normal_f32(w.data_ptr(), N * K, 40 + i, 0, 0.02)
+        qws.append(q4.QWeight.from_float(w))
+        del w
+        xb = torch.empty(K, dtype=torch.int16, device="cuda")
+        synth.dev_normal_bf16(xb.data_ptr(), K, 50 + i, 0, 1.0)
+        xs.append(xb.view(torch.bfloat16).view(1, K))
+        refs.append(q4.gemv(xs[-1], qws[-1], out_dtype=torch.float32))
+    ws = {}
+    for N, K in shapes:
+        need = max(q4.gemv_workspace_bytes(1, N2, K2) for N2, K2 in shapes if N2 == N)
+        ws[N] = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        for i, (N, K) in enumerate(shapes):
+            y = q4.gemv(xs[i], qws[i], out_dtype=torch.float32, ws=ws[N])
+            assert torch.equal(y, refs[i]), (N, K)
+    torch.cuda.synchronize()
+    assert q4.check() == q4.OK
+    for N, buf in ws.items():
+        cnt = buf[:((N + 63) // 64) * 4].view(torch.int32)
+        assert int(cnt.abs().sum()) == 0
+
+
 def test_gemv_short_workspace_rejected_and_nothing_written():
     import weight_only_int4_group_gb300 as q4
     N, K, M = 4096, 8192, 1

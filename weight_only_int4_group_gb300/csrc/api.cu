@@ -94,7 +94,7 @@ static q4_status gemv_common(const void *x, q4_dtype xt, int64_t M, int64_t N, i
     if (plan.maxc > 1) {
         a.count = static_cast<unsigned int *>(workspace);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                              counters_bytes(plan.nrb));
+                                              gemv_counter_bytes(N));
     }
     a.wait_ns = wait_ns;
     a.err = d->err;

@@ -215,7 +215,9 @@ struct GemvPlan {
 };
 
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
-size_t counters_bytes(int nrb);  // counter block at the start of the workspace
+// Counter block at the start of the workspace: one u32 arrival counter per
+// 64 output rows (more than the row blocks need), padded to 256 bytes.
+size_t gemv_counter_bytes(int64_t N);
 cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,

@@ -783,9 +783,9 @@ static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, F &&f)
     return two ? f(Kern<PATH_MMA, 2, 0, true>{}) : f(Kern<PATH_MMA, 1, 0, true>{});
 }
 
-size_t counters_bytes(int nrb)
+size_t gemv_counter_bytes(int64_t N)
 {
-    return ((static_cast<size_t>(nrb) * sizeof(unsigned int) + 255) / 256) * 256;
+    return ((static_cast<size_t>((N + 63) / 64) * sizeof(unsigned int) + 255) / 256) * 256;
 }
 
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
@@ -825,7 +825,7 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
         if (c1 - c0 + 1 > maxc) maxc = static_cast<int>(c1 - c0 + 1);
     }
     p.maxc = maxc;
-    p.workspace = maxc > 1 ? counters_bytes(p.nrb) + static_cast<size_t>(p.nrb) * maxc * RB * 16 *
+    p.workspace = maxc > 1 ? gemv_counter_bytes(N) + static_cast<size_t>(p.nrb) * maxc * RB * 16 *
                                                          static_cast<size_t>(M) * sizeof(float)
                            : 0;
     return p;

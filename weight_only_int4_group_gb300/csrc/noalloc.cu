@@ -73,8 +73,7 @@ extern "C" q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int6
     if (need > 0) {
         // The arrival counters (one u32 per 64 output rows, padded to 256
         // bytes, at the start of the workspace) must start at zero.
-        const size_t rows64 = static_cast<size_t>((N + 63) / 64);
-        const size_t counters = ((rows64 * sizeof(unsigned int) + 255) / 256) * 256;
+        const size_t counters = q4::gemv_counter_bytes(N);
         err = cudaMemsetAsync(scratch, 0, counters < need ? counters : need,
                               reinterpret_cast<cudaStream_t>(stream));
         if (err != cudaSuccess) return Q4_ERR_CUDA;
