@@ -214,11 +214,12 @@ __host__ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64
 
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
 // XSPLIT: f32 activations carried as bf16 hi + bf16 lo (two MMAs per step).
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG>
+// ONE: M = 1 known at compile time (unused MMA columns skipped).
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
     constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
-    const int xrows = XSTAGED ? a.M : 0;
+    const int xrows = XSTAGED ? (ONE ? 1 : a.M) : 0;
     const int SB = stage_bytes(MODE, xrows);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ofree + 1);
     float *after = reinterpret_cast<float *>(smem + NSTG * SB + CTRL_BYTES);
     float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
-    const int MSR = (MODE == PATH_FMA) ? 1 : a.M;  // red row stride
+    const int MSR = (MODE == PATH_FMA || ONE) ? 1 : a.M;  // red row stride
     float *out = red + W * RB * 16 * MSR;          // [RB * 16 rows][M]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         // outputs and the workspace may belong to the previous kernel
         grid_dep_wait();
         if (beg < end) {
-            const int Mo = (MODE == PATH_FMA) ? 1 : a.M;
+            const int Mo = (MODE == PATH_FMA || ONE) ? 1 : a.M;
             const int64_t slab = static_cast<int64_t>(RB * 16) * a.M;  // one contributor's partial
             const int rb_first = static_cast<int>(beg / NS), rb_last = static_cast<int>((end - 1) / NS);
             for (int rb = rb_first, e = 0; rb <= rb_last; ++rb, ++e) {
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // them only after it has completed.
     grid_dep_wait();
     const int gq = lane >> 2, t = lane & 3;
-    const int M = a.M;
+    const int M = ONE ? 1 : a.M;
     const int MS = MSR;
     const int Mo = (MODE == PATH_FMA) ? 1 : M;
     float *mypairs = after + warp * WARP_PAIR_FLOATS;  // FMA
@@ -482,14 +483,16 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         const uint8_t *stage = ring + slot * SB;
         const uint8_t *wtiles = stage + warp * TILE_BYTES;
         if (XSTAGED) {
-            const uint8_t *xs = stage + TILES_BYTES + gq * XROW + warp * G * 2 + 4 * t;
+            // Lanes of batch rows >= M read row M - 1: their MMA columns are
+            // never stored, and an MMA column depends on its own B column
+            // only.  An idle warp's reads stay inside the stage too.
+            const int xr = gq < M ? gq : M - 1;
+            const uint8_t *xs = stage + TILES_BYTES + xr * XROW + warp * G * 2 + 4 * t;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    bcur[0][j][h] = (gq < M && active)
-                                        ? *reinterpret_cast<const uint32_t *>(xs + 32 * j + 16 * h)
-                                        : 0u;
+                    bcur[0][j][h] = *reinterpret_cast<const uint32_t *>(xs + 32 * j + 16 * h);
         }
 
         if (active && MODE == PATH_FMA) {
@@ -639,15 +642,21 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 }
 #pragma unroll
                 for (int i = 0; i < TI; ++i) {
-                    const float zg = OFF + static_cast<float>(zp[i] & 0xFFu);
-                    const float zg8 = OFF + static_cast<float>(zp[i] >> 8);
+                    // OFF + zero: the byte under the exponent of 2^23, one
+                    // permute and one add each
+                    const float zg = __uint_as_float(__byte_perm(zp[i], 0x4B000000u, 0x7540)) -
+                                     (8388608.0f - OFF);
+                    const float zg8 = __uint_as_float(__byte_perm(zp[i], 0x4B000000u, 0x7541)) -
+                                      (8388608.0f - OFF);
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         float *ya = yacc[r0 + i][n];
                         ya[0] = fmaf(sp[i].x, fmaf(-zg, S[n][0], d[i][n][0]), ya[0]);
-                        ya[1] = fmaf(sp[i].x, fmaf(-zg, S[n][1], d[i][n][1]), ya[1]);
                         ya[2] = fmaf(sp[i].y, fmaf(-zg8, S[n][0], d[i][n][2]), ya[2]);
-                        ya[3] = fmaf(sp[i].y, fmaf(-zg8, S[n][1], d[i][n][3]), ya[3]);
+                        if (!ONE) {  // second MMA column: batch rows 2t + 1
+                            ya[1] = fmaf(sp[i].x, fmaf(-zg, S[n][1], d[i][n][1]), ya[1]);
+                            ya[3] = fmaf(sp[i].y, fmaf(-zg8, S[n][1], d[i][n][3]), ya[3]);
+                        }
                     }
                 }
             }
@@ -718,7 +727,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 }
 
 // -------------------------------------------------------------------- host
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE>
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false>
 struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     static int smem(int M)
@@ -734,7 +743,7 @@ struct Kern {
             *blocks_per_sm = cached[dev][M];
             return cudaSuccess;
         }
-        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG>;
+        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE>;
         if (!attr[dev]) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem(NSTG == NSTAGE ? 16 : 1));
@@ -761,7 +770,7 @@ struct Kern {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG>, a);
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE>, a);
     }
 };
 
@@ -773,11 +782,13 @@ static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, F &&f)
     // two CTAs per SM
     const bool two = M > 8;
     if (xt == Q4_F16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3>{});
+        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3, true>{});
+        if (M == 1) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, true>{});
         return two ? f(Kern<PATH_MMA, 2, 1, false>{}) : f(Kern<PATH_MMA, 1, 1, false>{});
     }
     if (xt == Q4_BF16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3>{});
+        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3, true>{});
+        if (M == 1) return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true>{});
         return two ? f(Kern<PATH_MMA, 2, 0, false>{}) : f(Kern<PATH_MMA, 1, 0, false>{});
     }
     return two ? f(Kern<PATH_MMA, 2, 0, true>{}) : f(Kern<PATH_MMA, 1, 0, true>{});
