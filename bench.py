@@ -347,9 +347,12 @@ def main():
                     help="NxK: time one GEMV shape alone (small-case mode for profilers)")
     ap.add_argument("--reps", type=int, default=3, help="launches in --case mode")
     ap.add_argument("--gemm-case", default=None, help="MxNxK: time one q4_gemm shape alone")
+    ap.add_argument("--quantize-case", default=None, help="NxK: time q4_quantize on one shape")
     args = ap.parse_args()
     if args.case:
         return single_case(args)
+    if args.quantize_case:
+        return quantize_case(args)
     if args.gemm_case:
         return gemm_case(args)
     if args.warmup < 3:
@@ -621,6 +624,41 @@ def single_case(args) -> int:
     nb = algo_bytes(M, N, K)
     print(json.dumps({"case": f"{N}x{K}", "M": M, "path": args.path, "copies": copies,
                       "launches": copies + args.reps, "us_per_call": round(t * 1e6, 2),
+                      "GB/s": round(nb / t / 1e9, 1)}), flush=True)
+    return 0
+
+
+def quantize_case(args) -> int:
+    """q4_quantize on one N x K f32 matrix (device-generated), `reps` launches
+    after one warm-up, printed as a plain JSON line."""
+    import torch
+
+    import synth
+    import weight_only_int4_group_gb300 as q4
+    N, K = (int(v) for v in args.quantize_case.lower().split("x"))
+    dev = torch.device("cuda")
+    w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    synth.dev_normal_f32(w.data_ptr(), N * K, 99, 0, SIGMA)
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    scale = torch.empty((N, K // 128), dtype=torch.float32, device=dev)
+    zero = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
+    lib = q4.lib()
+
+    def run():
+        rc = lib.q4_quantize(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(),
+                             zero.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == q4.OK, rc
+    run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        run()
+    b.record()
+    b.synchronize()
+    t = a.elapsed_time(b) / 1e3 / args.reps
+    nb = 4 * N * K + N * K // 2 + 5 * N * K // 128
+    print(json.dumps({"quantize_case": f"{N}x{K}", "us": round(t * 1e6, 2),
                       "GB/s": round(nb / t / 1e9, 1)}), flush=True)
     return 0
 

@@ -51,6 +51,34 @@ def test_quantize_bit_exact(N, K):
     assert np.array_equal(z.cpu().numpy(), zo)
 
 
+def test_quantize_near_tie_quotients():
+    """Weights whose quotient w / scale lies within a few ulps of a rounding
+    boundary n + 1/2 (both sides): the codes must follow the IEEE f32
+    quotient exactly."""
+    import weight_only_int4_group_gb300 as q4
+    rng = np.random.default_rng(17)
+    N, K = 64, 1024
+    W = np.empty((N, K), dtype=np.float32)
+    for r in range(N):
+        for g in range(K // 128):
+            lo = -np.float32(rng.uniform(0.01, 1.0))
+            hi = np.float32(rng.uniform(0.01, 1.0))
+            s = np.float32(np.float32(hi - lo) / np.float32(15.0))
+            n = rng.integers(-7, 7, 126).astype(np.float32)
+            w = np.float32((n + np.float32(0.5)) * s)
+            steps = rng.integers(-3, 4, 126)
+            for i, k in enumerate(steps):  # a few ulps either way
+                for _ in range(abs(int(k))):
+                    w[i] = np.nextafter(w[i], np.float32(np.inf if k > 0 else -np.inf))
+            w = np.clip(w, lo, hi)
+            W[r, g * 128:(g + 1) * 128] = np.concatenate([[lo, hi], w])
+    p, s_, z = q4.quantize(dev_f32(W))
+    po, so, zo = oracle.load().quantize(W)
+    assert np.array_equal(s_.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zo)
+    assert np.array_equal(p.cpu().numpy(), po)
+
+
 def test_quantize_page_program():
     import weight_only_int4_group_gb300 as q4
     w, _ = synth.page_program()

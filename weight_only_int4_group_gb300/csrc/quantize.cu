@@ -11,9 +11,50 @@
 
 namespace q4 {
 
+// Warp-wide minimum / maximum of one f32 per lane (exact selections).
+__device__ __forceinline__ float warp_min(float v)
+{
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Code of one weight: clamp(round(w / s) + z, 0, 15) with the quotient of
+// IEEE f32 division and ties away from zero, for |w / s| <= 16.
+// The product qa = w * r with the rounded reciprocal r differs from the exact
+// quotient by at most 2^-19 there (two roundings of relative 2^-24 on a value
+// below 16), and the IEEE quotient by at most 2^-20.  Adding 1.5 * 2^23
+// rounds qa to the nearest integer n (its bits minus those of 1.5 * 2^23 are
+// n); when qa - n lies within 1/2 - 2^-16 of zero, both quotients round to n
+// under any tie rule.  Otherwise (a quotient near n + 1/2, or a non-finite
+// product) the division is done.
+__device__ __forceinline__ int code_of(float w, float s, float r, int z)
+{
+    const float qa = __fmul_rn(w, r);
+    const float t = __fadd_rn(qa, 12582912.0f);
+    const float rem = __fsub_rn(qa, __fsub_rn(t, 12582912.0f));
+    int q;
+    if (fabsf(rem) < 0.5f - 0x1p-16f)  // false for NaN
+        q = __float_as_int(t) - 0x4B400000;
+    else
+        q = static_cast<int>(roundf(__fdiv_rn(w, s)));
+    q += z;
+    return q < 0 ? 0 : (q > 15 ? 15 : q);
+}
+
 // One warp per group of 128 weights: each lane holds 4 consecutive weights
-// (one 16-byte load), min/max by butterfly shuffles (exact, order-free),
-// then every lane quantizes its 4 weights and stores 2 packed bytes.
+// (one 16-byte load), warp-wide min/max (exact, order-free), then every lane
+// quantizes its 4 weights and stores 2 packed bytes.  A warp takes GPW groups
+// per pass, loading all of them before computing (so that enough loads are
+// in flight to keep HBM busy) and computing their scales in one go.
+constexpr int GPW = 4;
+
 __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, int64_t ngroups,
                                                   uint8_t *__restrict__ packed,
                                                   float *__restrict__ scale,
@@ -21,35 +62,50 @@ __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, i
 {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t gi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         gi < ngroups; gi += nwarps) {
-        const float4 v = __ldcs(reinterpret_cast<const float4 *>(w + gi * G) + lane);
-        float lo = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
-        float hi = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    for (int64_t g0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * GPW;
+         g0 < ngroups; g0 += nwarps * GPW) {
+        float4 vv[GPW];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        for (int u = 0; u < GPW; ++u)
+            vv[u] = g0 + u < ngroups ? __ldcs(reinterpret_cast<const float4 *>(w + (g0 + u) * G) + lane)
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        // group ranges; then lane u (< GPW) computes group u's scale, zero
+        // and reciprocal, once for all lanes, and broadcasts them
+        float mylo = 0.0f, myhi = 0.0f;
+#pragma unroll
+        for (int u = 0; u < GPW; ++u) {
+            const float4 v = vv[u];
+            const float lo = warp_min(fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+            const float hi = warp_max(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            if (lane == u) {
+                mylo = lo;
+                myhi = hi;
+            }
         }
         // keep 0 exactly representable
-        lo = fminf(lo, 0.0f);
-        hi = fmaxf(hi, 0.0f);
-        const float s = (hi > lo) ? __fdiv_rn(__fsub_rn(hi, lo), 15.0f) : 1.0f;
-        const float z = fminf(fmaxf(roundf(__fdiv_rn(-lo, s)), 0.0f), 15.0f);
-
-        uint32_t q[4];
-        const float e[4] = {v.x, v.y, v.z, v.w};
+        mylo = fminf(mylo, 0.0f);
+        myhi = fmaxf(myhi, 0.0f);
+        const float mys = (myhi > mylo) ? __fdiv_rn(__fsub_rn(myhi, mylo), 15.0f) : 1.0f;
+        const float myz = fminf(fmaxf(roundf(__fdiv_rn(-mylo, mys)), 0.0f), 15.0f);
+        const float myr = __frcp_rn(mys);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float c = fminf(fmaxf(__fadd_rn(roundf(__fdiv_rn(e[i], s)), z), 0.0f), 15.0f);
-            q[i] = static_cast<uint32_t>(c);
-        }
-        // flat index gi*128 + 4*lane + i: even index in the low nibble
-        const uint16_t two = static_cast<uint16_t>(q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12));
-        reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = two;
-        if (lane == 0) {
-            scale[gi] = s;
-            zero[gi] = static_cast<uint8_t>(z);
+        for (int u = 0; u < GPW; ++u) {
+            const int64_t gi = g0 + u;
+            if (gi >= ngroups) break;
+            const float4 v = vv[u];
+            const float sc = __shfl_sync(0xffffffffu, mys, u);
+            const float r = __shfl_sync(0xffffffffu, myr, u);
+            const int zi = static_cast<int>(__shfl_sync(0xffffffffu, myz, u));
+            // flat index gi*128 + 4*lane + i: even index in the low nibble
+            const uint32_t two = static_cast<uint32_t>(code_of(v.x, sc, r, zi)) |
+                                 (static_cast<uint32_t>(code_of(v.y, sc, r, zi)) << 4) |
+                                 (static_cast<uint32_t>(code_of(v.z, sc, r, zi)) << 8) |
+                                 (static_cast<uint32_t>(code_of(v.w, sc, r, zi)) << 12);
+            reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = static_cast<uint16_t>(two);
+            if (lane == u) {
+                scale[gi] = mys;
+                zero[gi] = static_cast<uint8_t>(myz);
+            }
         }
     }
 }
@@ -206,7 +262,8 @@ cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packe
                             uint8_t *zero, cudaStream_t s)
 {
     const int64_t ngroups = N * K / G;
-    k_quantize<<<grid_for(ngroups * 32, 256), 256, 0, s>>>(w, ngroups, packed, scale, zero);
+    k_quantize<<<grid_for((ngroups + GPW - 1) / GPW * 32, 256), 256, 0, s>>>(w, ngroups, packed,
+                                                                             scale, zero);
     return cudaGetLastError();
 }
 
