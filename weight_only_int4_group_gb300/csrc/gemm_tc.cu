@@ -6,19 +6,22 @@
 // same pass (page "LLM Quantization Architecture in Depth", "Kernels and
 // memory layout"); the fp weights never reach HBM.
 //
-// One persistent CTA per SM, 10 warps with fixed roles:
+// One persistent CTA per SM, 14 warps with fixed roles:
 //   warp 0     producer: activation tiles by 2-D tensor TMA (128-byte
 //              swizzle) and packed weight tiles by 1-D bulk copies;
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma;
-//   warps 2-5  dequantize: codes -> bf16 (or f16) w_hat = (q - zero) * scale,
-//              written in the K-major 128-byte-swizzled layout the MMA reads;
-//   warps 6-9  epilogue: tcgen05.ld of the accumulators -> bf16/f16 ->
-//              swizzled staging -> 2-D tensor TMA store.
-// CTA tile: 256 rows of X (two M=128 MMAs sharing one dequantized weight tile,
-// so each weight tile is dequantized once per 256 tokens) x 128 weight rows,
-// K in stages of 64.  Accumulators: 2 x 128 x 128 f32 per tile in tensor
-// memory, double-buffered (512 columns) so the epilogue of one tile overlaps
-// the MMAs of the next.  Every barrier wait is bounded; on expiry the CTA
+//   warps 2-9  dequantize, one 16-row tile each: codes -> bf16 (or f16)
+//              w_hat = (q - zero) * scale, written in the K-major
+//              128-byte-swizzled layout the MMA reads;
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators -> bf16/f16 ->
+//              coalesced stores (32 consecutive outputs of one token per
+//              warp instruction).
+// CTA tile: 128 weight rows x 256 tokens, K in stages of 64.  The MMA computes
+// the transposed product Y^T = W_hat * X^T: A = the dequantized weight tile
+// (128 rows), B = the 256 activation rows, one 128 x 256 x 16 MMA per 16 k,
+// so each weight tile is dequantized once per 256 tokens.  Accumulator:
+// 128 lanes x 256 f32 columns in tensor memory, double-buffered (512
+// columns) so the epilogue of one tile overlaps the MMAs of the next.  Every barrier wait is bounded; on expiry the CTA
 // raises the device error word, stops, drains its copies and MMAs, frees its
 // tensor memory and returns.
 #include <cuda.h>
@@ -32,7 +35,7 @@ namespace q4 {
 namespace gm {
 
 constexpr int BM = 256, SUB = 128, BN = 128, BK = 64;
-constexpr int NA = 3;   // activation stages
+constexpr int NA = 4;   // activation stages (latency of the L2 reads of X)
 constexpr int NBS = 3;  // dequantized-weight stages
 constexpr int NC = 2;   // packed-code stages (one group = two k stages)
 constexpr int RT = BN / TILE_ROWS;         // 8 row tiles per weight tile
@@ -40,19 +43,16 @@ constexpr int A_BOX = SUB * BK * 2;        // 16384: one 128 x 64 activation box
 constexpr int A_STAGE = 2 * A_BOX;         // 32768
 constexpr int B_STAGE = BN * BK * 2;       // 16384
 constexpr int C_STAGE = RT * TILE_BYTES;   // 8832
-constexpr int E_BOX = 32 * 128;            // 32 rows x 128 bytes of output
-constexpr int E_WARP = 2 * E_BOX;          // 64 output columns x 2 boxes = 128 columns
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NA * A_STAGE;
 constexpr int OFF_C = OFF_B + NBS * B_STAGE;
-constexpr int OFF_E = ((OFF_C + NC * C_STAGE + 1023) / 1024) * 1024;
-constexpr int OFF_BAR = OFF_E + 4 * E_WARP;
+constexpr int OFF_BAR = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;
 constexpr int SMEM_USED = OFF_BAR + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
-constexpr int THREADS = 320;
+constexpr int THREADS = 448;
 constexpr uint32_t TMEM_COLS = 512;
 
-static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0 && OFF_E % 1024 == 0, "alignment");
+static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0, "alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
 
 // ----------------------------------------------------------------- PTX
@@ -65,21 +65,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(smem_u32(src))
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -113,10 +98,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
 }
 
 // Instruction descriptor, kind::f16: f32 accumulate, A/B bf16 (ab = 1) or
-// f16 (ab = 0), both K-major, M = 128, N = 128.
+// f16 (ab = 0), both K-major, M = 128, N = 256.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab)
 {
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -168,6 +153,7 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t p, float neg_z, float 
 
 struct Args {
     const uint8_t *qw;
+    void *y;
     int M, N, K;
     int mt, nt;  // tiles along M (256 rows) and N (128 rows)
     uint64_t wait_ns;
@@ -178,8 +164,7 @@ struct Args {
 // YF16: outputs are f16, else bf16.
 template <bool F16, bool YF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
-           const Args a)
+    k_gemm(const __grid_constant__ CUtensorMap tmx, const Args a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -187,7 +172,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *sA = smem + OFF_A;
     uint8_t *sB = smem + OFF_B;
     uint8_t *sC = smem + OFF_C;
-    uint8_t *sE = smem + OFF_E;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full_a = bar, *empty_a = bar + NA;
     uint64_t *full_b = bar + 2 * NA, *empty_b = full_b + NBS;
@@ -209,12 +193,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&empty_a[i], 1);
         }
         for (int i = 0; i < NBS; ++i) {
-            mbar_init(&full_b[i], 4);
+            mbar_init(&full_b[i], 8);
             mbar_init(&empty_b[i], 1);
         }
         for (int i = 0; i < NC; ++i) {
             mbar_init(&full_c[i], 1);
-            mbar_init(&empty_c[i], 4);
+            mbar_init(&empty_c[i], 8);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -286,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
+                const uint32_t d = tmem + buf * 256;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int sa = ia % NA, sb = ib % NBS;
                     if (!mbar_wait_bounded(&full_a[sa], (ia / NA) & 1, abort_flag, a.wait_ns, a.err) ||
@@ -295,14 +279,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + sa * A_STAGE), a1 = a0 + A_BOX;
-                    const uint32_t b0 = smem_u32(sB + sb * B_STAGE);
+                    // A operand: the weight tile; B operand: the 256
+                    // activation rows (two TMA boxes, contiguous)
+                    const uint32_t xa = smem_u32(sA + sa * A_STAGE);
+                    const uint32_t wb = smem_u32(sB + sb * B_STAGE);
 #pragma unroll
                     for (int k16 = 0; k16 < BK / 16; ++k16) {
                         const uint32_t acc = (ks > 0 || k16 > 0) ? 1u : 0u;
-                        const uint64_t bd = sw128_desc(b0 + 32 * k16);
-                        mma_f16(d0, sw128_desc(a0 + 32 * k16), bd, idesc, acc);
-                        mma_f16(d1, sw128_desc(a1 + 32 * k16), bd, idesc, acc);
+                        mma_f16(d, sw128_desc(wb + 32 * k16), sw128_desc(xa + 32 * k16), idesc, acc);
                     }
                     issued = true;
                     mma_commit(&empty_a[sa]);
@@ -319,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_wait_bounded(drain, 0, abort_flag, a.wait_ns, a.err, false);
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------------ dequantize
         const int d = warp - 2, gq = lane >> 2, t = lane & 3;
         int ib = 0, ic = 0;
@@ -340,8 +324,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 uint8_t *bst = sB + sb * B_STAGE;
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int r = 2 * d + rr;
+                for (int rr = 0; rr < 1; ++rr) {
+                    const int r = d + rr;
                     if (r < nrt) {
                         const uint8_t *ct = sC + sc * C_STAGE + r * TILE_BYTES;
                         const uint4 cw = *reinterpret_cast<const uint4 *>(ct + h * 512 + 16 * lane);
@@ -379,8 +363,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------ epilogue
-        const int p = warp & 3;  // tensor-memory lane quarter this warp may read
-        uint8_t *stg = sE + (warp - 6) * E_WARP;
+        // Warp p reads tensor-memory lanes 32p..32p+31 (weight rows n0 + 32p
+        // + lane); each 32-column load gives a lane 32 consecutive tokens, and
+        // for every token the warp stores 32 consecutive outputs (64 bytes).
+        const int p = warp & 3;
         int tt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
@@ -392,52 +378,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
+            const int n = n0 + 32 * p + lane;
+            uint16_t *ycol = reinterpret_cast<uint16_t *>(a.y) + n;
 #pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
-                // the previous store must have finished reading the staging buffer
-                if (lane == 0) bulk_wait_read0();
-                __syncwarp();
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * p) << 16) + buf * 256 + sub * 128 + 32 * c, v);
-                    uint32_t o[16];
+            for (int c = 0; c < BM / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * p) << 16) + buf * 256 + 32 * c, v);
+                const int mb = m0 + 32 * c;
+                if (mb >= a.M) break;  // warp-uniform
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 f = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        if (YF16) {
-                            const __half2 hh = __float22half2_rn(f);
-                            o[i] = *reinterpret_cast<const uint32_t *>(&hh);
-                        } else {
-                            const __nv_bfloat162 bb = __float22bfloat162_rn(f);
-                            o[i] = *reinterpret_cast<const uint32_t *>(&bb);
-                        }
+                for (int j = 0; j < 32; ++j) {
+                    const float f = __uint_as_float(v[j]);
+                    uint16_t o;
+                    if (YF16) {
+                        const __half h = __float2half_rn(f);
+                        o = *reinterpret_cast<const uint16_t *>(&h);
+                    } else {
+                        const __nv_bfloat16 bb = __float2bfloat16_rn(f);
+                        o = *reinterpret_cast<const uint16_t *>(&bb);
                     }
-                    // columns 32c..32c+31 of this lane's row: box c/2, chunks 4(c%2)..+3
-                    uint8_t *rowp = stg + (c >> 1) * E_BOX + lane * 128;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chunk = (4 * (c & 1) + q) ^ (lane & 7);
-                        *reinterpret_cast<uint4 *>(rowp + chunk * 16) =
-                            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int row = m0 + sub * SUB + 32 * p;
-                    if (row < a.M) {
-                        tma_store_2d(&tmy, n0, row, stg);
-                        if (n0 + 64 < a.N) tma_store_2d(&tmy, n0 + 64, row, stg + E_BOX);
-                    }
-                    bulk_commit();
+                    if (mb + j < a.M && n < a.N) ycol[static_cast<int64_t>(mb + j) * a.N] = o;
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
-        if (lane == 0) bulk_wait0();
     }
 
     tc_fence_before();
@@ -486,13 +452,11 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
     *cerr = cudaSuccess;
     const bool f16 = (xt == Q4_F16);
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tmx, tmy;
+    CUtensorMap tmx;
     if (!make_map(&tmx, x, dt, K, M, K * 2, BK, SUB)) return Q4_ERR_UNSUPPORTED;
-    const CUtensorMapDataType dy = (yt == Q4_F16) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_map(&tmy, y, dy, N, M, N * 2, 64, 32)) return Q4_ERR_UNSUPPORTED;
     Args a{};
     a.qw = static_cast<const uint8_t *>(qw);
+    a.y = y;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
@@ -514,7 +478,7 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
         if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
         configured[variant][dev] = true;
     }
-    kern<<<grid, THREADS, SMEM_ALLOC, s>>>(tmx, tmy, a);
+    kern<<<grid, THREADS, SMEM_ALLOC, s>>>(tmx, a);
     *cerr = cudaGetLastError();
     return *cerr == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
