@@ -83,6 +83,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// One non-blocking probe of an mbarrier phase (for latency-critical waiters
+// that poll instead of being suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
@@ -95,14 +109,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 // another role of the CTA has already aborted.  Never spins without bound.
 // With honor_abort == false (used to drain copies already in flight before
 // a CTA exits) only the time bound ends the wait.
+// With poll == true the waiter probes without being suspended (reacts
+// sooner, takes issue slots meanwhile).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   volatile int *abort_flag, uint64_t limit_ns,
-                                                  unsigned int *err, bool honor_abort = true)
+                                                  unsigned int *err, bool honor_abort = true,
+                                                  bool poll = false)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (honor_abort && *abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
                 const int buf = tt & 1;
                 if (tt >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((tt >> 1) - 1) & 1, abort_flag,
-                                                  a.wait_ns, a.err)) {
+                                                  a.wait_ns, a.err, true, true)) {
                     ok = false;
                     break;
                 }
@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d = tmem + buf * 256;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int sa = ia % NA, sb = ib % NBS;
-                    if (!mbar_wait_bounded(&full_a[sa], (ia / NA) & 1, abort_flag, a.wait_ns, a.err) ||
-                        !mbar_wait_bounded(&full_b[sb], (ib / NBS) & 1, abort_flag, a.wait_ns, a.err)) {
+                    if (!mbar_wait_bounded(&full_a[sa], (ia / NA) & 1, abort_flag, a.wait_ns, a.err, true, true) ||
+                        !mbar_wait_bounded(&full_b[sb], (ib / NBS) & 1, abort_flag, a.wait_ns, a.err, true, true)) {
                         ok = false;
                         break;
                     }
