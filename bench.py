@@ -523,6 +523,30 @@ def extra_rows(q4, torch, work, pk) -> dict:
                              "weight+scale GB/s": round((N * K // 2 + 5 * N * K // 128) / t / 1e9, 1),
                              "TFLOP/s": round(2 * M * N * K / t / 1e12, 3)}
             del g
+        # M = 32: the large-M GEMM, and two M = 16 GEMVs for comparison
+        M = 32
+        x = torch.empty(M * K, dtype=torch.int16, device=dev)
+        synth.dev_normal_bf16(x.data_ptr(), M * K, 4242 + M, 0, 1.0)
+        x = x.view(torch.bfloat16).view(M, K)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsp = torch.zeros(max(q4.gemv_workspace_bytes(16, N, K), 256), dtype=torch.uint8, device=dev)
+
+        def run_gemm():
+            for l in range(L):
+                q4.gemm(x, qws[l], out=y)
+
+        def run_two():
+            for l in range(L):
+                q4.gemv(x[:16], qws[l], out=y[:16], ws=wsp)
+                q4.gemv(x[16:], qws[l], out=y[16:], ws=wsp)
+        b = algo_bytes(M, N, K)
+        for rname, fn in (("M=32 q4_gemm", run_gemm), ("M=32 as 2 x M=16 q4_gemv", run_two)):
+            g = graph_of(torch, fn)
+            t = time_graph(torch, g, reps=5) / L
+            res[rname] = {"us_per_call": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                          "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4),
+                          "TFLOP/s": round(2 * M * N * K / t / 1e12, 3)}
+            del g
         # M = 1 through each kernel explicitly (AUTO picks the tensor-core one)
         x = torch.empty(K, dtype=torch.int16, device=dev)
         synth.dev_normal_bf16(x.data_ptr(), K, 4242, 0, 1.0)
@@ -541,6 +565,93 @@ def extra_rows(q4, torch, work, pk) -> dict:
             del g
         sweep[name] = res
     rows["mlp_sweep"] = sweep
+
+    # the decode step at M = 8 on the same weights (80 layers, one graph)
+    M = 8
+    import synth
+    xs, ys, ws8 = [], [], {}
+    for _, N, K in LAYER_SHAPES:
+        xb = torch.empty(M * K, dtype=torch.int16, device=dev)
+        synth.dev_normal_bf16(xb.data_ptr(), M * K, 808 + K, 0, 1.0)
+        xs.append(xb.view(torch.bfloat16).view(M, K))
+        ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
+        need = max(q4.gemv_workspace_bytes(M, N2, K2) for _, N2, K2 in LAYER_SHAPES if N2 == N)
+        ws8.setdefault(N, torch.zeros(max(need, 256), dtype=torch.uint8, device=dev))
+
+    def step8():
+        for l in range(L):
+            for i, (_, N, K) in enumerate(LAYER_SHAPES):
+                q4.gemv(xs[i], work.qw[l][i], out=ys[i], ws=ws8[N])
+    g = graph_of(torch, step8)
+    t = time_graph(torch, g, reps=3)
+    b = L * sum(algo_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
+    rows["decode_step_M8"] = {"layers": L, "ms_per_step": round(t * 1e3, 3),
+                              "GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
+    del g, xs, ys, ws8
+
+    # Llama-7B-shaped layer, M = 1 (qkv 12288x4096, o 4096x4096, gate and up
+    # 11008x4096 each, down 4096x11008; 0.1% of input channels x20): 8
+    # distinct layers per graph (0.87 GB, beyond L2), time per layer
+    shapes7 = [("qkv", 12288, 4096), ("o", 4096, 4096), ("gate", 11008, 4096), ("up", 11008, 4096),
+               ("down", 4096, 11008)]
+    L7 = 8
+    q7 = []
+    for l in range(L7):
+        mats = []
+        for i, (_, N, K) in enumerate(shapes7):
+            w = torch.empty((N, K), dtype=torch.float32, device=dev)
+            cols = torch.from_numpy(synth.outlier_columns(70 + i, K).astype("int64")).to(dev)
+            synth.dev_normal_f32(w.data_ptr(), N * K, 7000 + 10 * l + i, 0, SIGMA)
+            w[:, cols] *= 20.0
+            mats.append(q4.QWeight.from_float(w))
+            del w
+        q7.append(mats)
+    x7 = {}
+    for _, N, K in shapes7:
+        if K not in x7:
+            xb = torch.empty(K, dtype=torch.int16, device=dev)
+            synth.dev_normal_bf16(xb.data_ptr(), K, 707 + K, 0, 1.0)
+            x7[K] = xb.view(torch.bfloat16).view(1, K)
+    y7 = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for _, N, _ in shapes7]
+    ws7 = {N: torch.zeros(max(256, max(q4.gemv_workspace_bytes(1, N2, K2) for _, N2, K2 in shapes7
+                                       if N2 == N)), dtype=torch.uint8, device=dev)
+           for _, N, _ in shapes7}
+
+    def layer7():
+        for l in range(L7):
+            for i, (_, N, K) in enumerate(shapes7):
+                q4.gemv(x7[K], q7[l][i], out=y7[i], ws=ws7[N])
+    g = graph_of(torch, layer7)
+    t = time_graph(torch, g, reps=10) / L7
+    b = sum(algo_bytes(1, N, K) for _, N, K in shapes7)
+    rows["llama7b_layer_M1"] = {"us_per_layer": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                                "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4),
+                                "launches_per_layer": len(shapes7)}
+    del g, q7, x7, y7, ws7
+
+    # single GEMV, 4096 x 4096, the page's xorshift matrix, f32 x and y, M = 1:
+    # one copy repeated (L2-resident) and 48 copies rotated (0.44 GB, beyond L2)
+    W1, xv = synth.xorshift_matrix(4096, 4096)
+    w1 = torch.from_numpy(W1).to(dev)
+    q1 = q4.QWeight.from_float(w1)
+    del w1
+    x1 = torch.from_numpy(xv.reshape(1, -1)).to(dev)
+    y1 = torch.empty((1, 4096), dtype=torch.float32, device=dev)
+    copies = [q1] + [q4.QWeight(q1.data.clone(), 4096, 4096) for _ in range(47)]
+    ws1 = torch.zeros(max(q4.gemv_workspace_bytes(1, 4096, 4096), 256), dtype=torch.uint8, device=dev)
+    b = algo_bytes(1, 4096, 4096, xb=4, yb=4)
+    single = {}
+    for rname, seq in (("L2-resident (one copy)", [q1] * 48), ("rotated (48 copies)", copies)):
+        def run1():
+            for qq in seq:
+                q4.gemv(x1, qq, out=y1, ws=ws1)
+        g = graph_of(torch, run1)
+        t = time_graph(torch, g, reps=10) / len(seq)
+        single[rname] = {"us_per_call": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                         "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
+        del g
+    rows["single_4096x4096_f32"] = single
+    del copies, q1, x1, y1, ws1
 
     # large-M GEMM (prefill): 4096 tokens x 8192 x 28672, tcgen05 tensor cores
     Mg, Ng, Kg = 4096, 28672, 8192

@@ -118,7 +118,7 @@ q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
 
 /* Workspace bytes q4_gemv needs for this problem on the current device (0
  * when no split over K is used).  Layout: split-K arrival counters (one u32
- * per 64 output rows, padded to 256 B) followed by f32 partial sums.  The
+ * per 32 output rows, padded to 256 B) followed by f32 partial sums.  The
  * counter block must be zero before the first call (zero-fill the buffer
  * once after allocation); every completed call leaves it zero again.  One
  * workspace may serve successive calls with the same N (their counter

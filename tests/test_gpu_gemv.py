@@ -101,7 +101,7 @@ def test_gemv_deterministic_and_workspace_restored():
     assert torch.equal(y1, y2)
     if ws is not None:
         # the split-K arrival counters (the head of the workspace) are back to zero
-        cnt = ws[:((N + 63) // 64) * 4].view(torch.int32)
+        cnt = ws[:((N + 31) // 32) * 4].view(torch.int32)
         assert int(cnt.abs().sum()) == 0
 
 
@@ -133,7 +133,7 @@ def test_gemv_workspace_shared_by_calls_with_the_same_n():
     torch.cuda.synchronize()
     assert q4.check() == q4.OK
     for N, buf in ws.items():
-        cnt = buf[:((N + 63) // 64) * 4].view(torch.int32)
+        cnt = buf[:((N + 31) // 32) * 4].view(torch.int32)
         assert int(cnt.abs().sum()) == 0
 
 

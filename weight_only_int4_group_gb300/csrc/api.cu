@@ -160,14 +160,19 @@ size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K)
     if (M < 1 || M > Q4_GEMV_MAX_M || !sizes_ok(N, K)) return 0;
     const DevInfo *d = dev_info();
     if (!d) return 0;
-    // the larger of the two paths' needs, so one buffer serves either
-    const GemvPlan a = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                 Q4_BF16, PATH_AUTO, d->sm_count);
-    const GemvPlan b = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                 Q4_F32, PATH_AUTO, d->sm_count);
-    const GemvPlan c = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                 Q4_F32, M == 1 ? PATH_FMA : PATH_MMA, d->sm_count);
-    return std::max(a.workspace, std::max(b.workspace, c.workspace));
+    // the largest need over activation types and paths, so one buffer serves
+    // every call with this shape
+    size_t need = 0;
+    const q4_dtype types[3] = {Q4_BF16, Q4_F16, Q4_F32};
+    const int paths[3] = {PATH_AUTO, PATH_MMA, PATH_FMA};
+    for (q4_dtype t : types)
+        for (int p : paths) {
+            if (p == PATH_FMA && M != 1) continue;
+            const GemvPlan g = gemv_plan(static_cast<int>(M), static_cast<int>(N),
+                                         static_cast<int>(K), t, p, d->sm_count);
+            need = std::max(need, g.workspace);
+        }
+    return need;
 }
 
 q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,

@@ -228,12 +228,13 @@ struct GemvPlan {
     int grid;  // persistent CTAs
     int maxc;  // most CTAs sharing one row block (1: no partial sums)
     bool deep; // 3-stage ring (M = 1, 16-bit activations, many steps per CTA)
+    bool small;  // 2-tile row blocks (few steps per CTA)
     size_t workspace;
 };
 
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
 // Counter block at the start of the workspace: one u32 arrival counter per
-// 64 output rows (more than the row blocks need), padded to 256 bytes.
+// 32 output rows (at least one per row block), padded to 256 bytes.
 size_t gemv_counter_bytes(int64_t N);
 cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
 

@@ -7,7 +7,9 @@
 // turned into floating point in registers and never written back to memory.
 //
 // Work decomposition (stream-K): the output rows are cut into row blocks of
-// RB = 8 tiles (128 rows); each row block is a sequence of NS = ceil(NG/4)
+// RB = 8 tiles (128 rows; 2 tiles when 2 <= M <= 8 and 8-tile blocks would
+// give each CTA fewer than 4 steps); each row block is a sequence of
+// NS = ceil(NG/4)
 // steps, a step being 4 consecutive groups along K.  The nrb * NS items are
 // split into `grid` contiguous, equal ranges, one per persistent CTA (two
 // CTAs per SM).  A CTA accumulates the steps of a row block in registers and
@@ -55,11 +57,11 @@
 namespace q4 {
 
 constexpr int W = 4;        // consumer warps = groups per step
-constexpr int RB = 8;       // row tiles per row block
+constexpr int RB = 8;       // row tiles per row block (RB_SMALL for small problems)
+constexpr int RB_SMALL = 2;
 constexpr int NSTAGE = 2;   // ring depth (3 for the M = 1 tensor-core kernel on long runs)
 constexpr int THREADS = (W + 2) * 32;  // consumers, producer, epilogue
 constexpr int CONSUMERS = W * 32;
-constexpr int TILES_BYTES = RB * W * TILE_BYTES;  // 17664
 constexpr int XSTAGE_BYTES = W * G * 4;           // FMA: the step's activations (f32 worst case)
 constexpr int CTRL_BYTES = 128;                   // barriers + flags
 // FMA activation pairs, per warp: one record of 64 floats per lane class t,
@@ -67,23 +69,23 @@ constexpr int CTRL_BYTES = 128;                   // barriers + flags
 // groups in one wavefront; then the four sum records.
 constexpr int PAIR_STRIDE = 68;
 constexpr int WARP_PAIR_FLOATS = 4 * PAIR_STRIDE + 4 * 4;
-constexpr int RED_FLOATS_FMA = W * RB * 16;
 constexpr int MIN_BLOCKS = 2;  // CTAs per SM the shared memory budget is sized for
 
 constexpr int XROW = W * G * 2 + 16;  // MMA staged activations: one padded row per batch row
 
 // xrows: batch rows staged with each step (MMA, M <= 8); 0 otherwise
-__host__ __device__ constexpr int stage_bytes(int mode, int xrows)
+__host__ __device__ constexpr int stage_bytes(int mode, int xrows, int rb = RB)
 {
-    return mode == PATH_FMA ? TILES_BYTES + XSTAGE_BYTES
-                            : ((TILES_BYTES + xrows * XROW + 127) / 128) * 128;
+    return mode == PATH_FMA ? rb * W * TILE_BYTES + XSTAGE_BYTES
+                            : ((rb * W * TILE_BYTES + xrows * XROW + 127) / 128) * 128;
 }
 
-__host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms, int nstage = NSTAGE)
+__host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms, int nstage = NSTAGE,
+                                             int rb = RB)
 {
-    return nstage * stage_bytes(mode, xrows) + CTRL_BYTES +
-           (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + RED_FLOATS_FMA) * 4 : W * RB * 16 * ms * 4) +
-           RB * 16 * ms * 4;  // hand-off buffer of one row block
+    return nstage * stage_bytes(mode, xrows, rb) + CTRL_BYTES +
+           (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + W * rb * 16) * 4 : W * rb * 16 * ms * 4) +
+           rb * 16 * ms * 4;  // hand-off buffer of one row block
 }
 
 
@@ -215,12 +217,15 @@ __host__ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
 // XSPLIT: f32 activations carried as bf16 hi + bf16 lo (two MMAs per step).
 // ONE: M = 1 known at compile time (unused MMA columns skipped).
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE>
+// RBT: row tiles per row block.
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE, int RBT>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
+    constexpr int RB = RBT;
+    constexpr int TILES_BYTES = RBT * W * TILE_BYTES;
     constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     const int xrows = XSTAGED ? (ONE ? 1 : a.M) : 0;
-    const int SB = stage_bytes(MODE, xrows);
+    const int SB = stage_bytes(MODE, xrows, RBT);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTG * SB);
@@ -581,7 +586,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             const float OFF = ABT == 0 ? 128.0f : 1024.0f;
             // TI tiles at a time: TI * NT independent accumulator chains, plus
             // NT chains for the activation sums
-            constexpr int TI = (NT == 1) ? 4 : 2;
+            constexpr int TI0 = (NT == 1) ? 4 : 2;
+            constexpr int TI = TI0 < RB ? TI0 : RB;
             float S[NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -727,12 +733,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 }
 
 // -------------------------------------------------------------------- host
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false>
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false, int RBT = RB>
 struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     static int smem(int M)
     {
-        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG);
+        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG, RBT);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
     {
@@ -743,7 +749,7 @@ struct Kern {
             *blocks_per_sm = cached[dev][M];
             return cudaSuccess;
         }
-        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE>;
+        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT>;
         if (!attr[dev]) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem(NSTG == NSTAGE ? 16 : 1));
@@ -770,14 +776,19 @@ struct Kern {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE>, a);
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT>, a);
     }
 };
 
 template <typename F>
-static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, F &&f)
+static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, bool small, F &&f)
 {
     if (path == PATH_FMA) return f(Kern<PATH_FMA, 1, 0, false>{});
+    // small: 2-tile row blocks (2 <= M <= 8, 16-bit activations staged)
+    if (small && M >= 2 && M <= 8 && xt != Q4_F32) {
+        if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL>{});
+        return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL>{});
+    }
     // deep: M = 1 with 16-bit activations, where a 3-stage ring still fits
     // two CTAs per SM
     const bool two = M > 8;
@@ -796,7 +807,7 @@ static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, F &&f)
 
 size_t gemv_counter_bytes(int64_t N)
 {
-    return ((static_cast<size_t>((N + 63) / 64) * sizeof(unsigned int) + 255) / 256) * 256;
+    return ((static_cast<size_t>((N + 31) / 32) * sizeof(unsigned int) + 255) / 256) * 256;
 }
 
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
@@ -809,23 +820,34 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     // per step for the hi/lo split of each activation).
     if (path == PATH_AUTO) path = (M == 1 && xt == Q4_F32) ? PATH_FMA : PATH_MMA;
     p.path = path;
-    p.rb = RB;
     const int ntiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int NG = K / G;
     const int NS = (NG + W - 1) / W;
-    p.nrb = (ntiles + RB - 1) / RB;
     int dev = 0, per_sm = 1;
     cudaGetDevice(&dev);
-    dispatch(path, M, xt, false, [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    dispatch(path, M, xt, false, false,
+             [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 8: use
+    // 2-tile ones, so that steps are short and plentiful (measured faster
+    // there; at M = 1 the longer steps win).
+    const int64_t T8 = static_cast<int64_t>((ntiles + RB - 1) / RB) * NS;
+    p.small = T8 < 4 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 2 &&
+              M <= 8 && xt != Q4_F32;
+    if (p.small)
+        dispatch(path, M, xt, false, true,
+                 [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    p.rb = p.small ? RB_SMALL : RB;
+    p.nrb = (ntiles + p.rb - 1) / p.rb;
     const int64_t T = static_cast<int64_t>(p.nrb) * NS;
     const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
     p.grid = static_cast<int>(T < slots ? T : slots);
     // The 3-stage ring pays off once each CTA streams many steps; with only a
     // few, the deeper first wave of requests delays every CTA's first step.
-    p.deep = path == PATH_MMA && M == 1 && xt != Q4_F32 && T >= 8 * static_cast<int64_t>(p.grid);
+    p.deep = !p.small && path == PATH_MMA && M == 1 && xt != Q4_F32 &&
+             T >= 8 * static_cast<int64_t>(p.grid);
     if (p.deep) {  // same CTAs per SM, or keep the 2-stage ring
         int per_sm_deep = 0;
-        dispatch(path, M, xt, true,
+        dispatch(path, M, xt, true, false,
                  [&](auto k) { return decltype(k)::configure(dev, M, &per_sm_deep); });
         p.deep = per_sm_deep == per_sm;
     }
@@ -836,7 +858,7 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
         if (c1 - c0 + 1 > maxc) maxc = static_cast<int>(c1 - c0 + 1);
     }
     p.maxc = maxc;
-    p.workspace = maxc > 1 ? gemv_counter_bytes(N) + static_cast<size_t>(p.nrb) * maxc * RB * 16 *
+    p.workspace = maxc > 1 ? gemv_counter_bytes(N) + static_cast<size_t>(p.nrb) * maxc * p.rb * 16 *
                                                          static_cast<size_t>(M) * sizeof(float)
                            : 0;
     return p;
@@ -844,7 +866,7 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
 
 cudaError_t gemv_launch(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
 {
-    return dispatch(p.path, a.M, a.xt, p.deep,
+    return dispatch(p.path, a.M, a.xt, p.deep, p.small,
                     [&](auto k) { return decltype(k)::launch(p.grid, a, s); });
 }
 

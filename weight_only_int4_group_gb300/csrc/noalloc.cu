@@ -71,7 +71,7 @@ extern "C" q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int6
     void *scratch = scratch_for_current_device(&err);
     if (!scratch) return Q4_ERR_CUDA;
     if (need > 0) {
-        // The arrival counters (one u32 per 64 output rows, padded to 256
+        // The arrival counters (one u32 per 32 output rows, padded to 256
         // bytes, at the start of the workspace) must start at zero.
         const size_t counters = q4::gemv_counter_bytes(N);
         err = cudaMemsetAsync(scratch, 0, counters < need ? counters : need,
