@@ -146,8 +146,8 @@ q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
 /* Kernel choice for q4_gemv_path.  FMA: CUDA-core f32 FMAs on codes turned
  * into f32 in registers (M = 1 only).  MMA: m16n8k16 tensor-core MMAs with the
  * codes as bf16/f16 A fragments built in registers and the batch as the n
- * dimension.  AUTO (what q4_gemv uses): MMA, except FMA for f32 activations
- * at M = 1. */
+ * dimension (f32 activations as a bf16 high part plus a bf16 low part, two
+ * MMAs per fragment).  AUTO (what q4_gemv uses): MMA. */
 #define Q4_PATH_AUTO 0
 #define Q4_PATH_FMA 1
 #define Q4_PATH_MMA 2

@@ -47,7 +47,8 @@
 //     tensor-core MMA as bf16 pairs 128 + q (f16: 1024 + q) with one LOP3
 //     each; the activations are the B fragment (the batch is the MMA's n
 //     dimension).  For M <= 8 (bf16/f16) the producer copies the step's
-//     activation rows into the stage next to the tiles (rows padded by 16
+//     activation rows (f32 at M = 1 for f32 activations, split into hi + lo
+//     per step) into the stage next to the tiles (rows padded by 16
 //     bytes so the eight batch rows fall in different banks); otherwise each
 //     lane loads its B fragments from L2 one step ahead.  The group sums of the
 //     activations come from one extra MMA per k-step with an all-ones A
@@ -224,8 +225,11 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     constexpr int RB = RBT;
     constexpr int TILES_BYTES = RBT * W * TILE_BYTES;
     constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    // XS32: M = 1 f32 activations staged as f32 with the tiles (split into
+    // bf16 hi + lo per step); the FMA path stages the same way
+    constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
     const int xrows = XSTAGED ? (ONE ? 1 : a.M) : 0;
-    const int SB = stage_bytes(MODE, xrows, RBT);
+    const int SB = stage_bytes(XS32 ? PATH_FMA : MODE, xrows, RBT);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTG * SB);
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 // it; their activation copies follow the wait.
                 auto issue_x = [&](int slot, int g0, int ng) {
                     uint8_t *stage = ring + slot * SB;
-                    if (MODE == PATH_FMA)
+                    if (MODE == PATH_FMA || XS32)
                         bulk_g2s(stage + TILES_BYTES,
                                  static_cast<const uint8_t *>(a.x) + static_cast<int64_t>(g0) * G * xb,
                                  static_cast<uint32_t>(ng) * G * xb, &full[slot]);
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                     const int rt0 = rb * RB, nrt = min(RB, ntiles - rt0);
                     const int g0 = s * W, ng = min(W, NG - g0);
                     const uint32_t row_bytes = static_cast<uint32_t>(ng) * TILE_BYTES;
-                    const uint32_t xbytes = (MODE == PATH_FMA) ? static_cast<uint32_t>(ng) * G * xb
+                    const uint32_t xbytes = (MODE == PATH_FMA || XS32) ? static_cast<uint32_t>(ng) * G * xb
                                             : static_cast<uint32_t>(xrows) * ng * G * 2;
                     uint8_t *stage = ring + slot * SB;
                     mbar_arrive_expect_tx(&full[slot], row_bytes * nrt + xbytes);
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             }
         }
     };
-    if (MODE == PATH_MMA && !XSTAGED && beg < end)
+    if (MODE == PATH_MMA && !XSTAGED && !XS32 && beg < end)
         load_b(static_cast<int>(beg % NS) * W + warp, bcur, blo);
 
     float yacc[RB][NT][4];
@@ -481,12 +485,26 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             ok = false;
             break;
         }
-        if (MODE == PATH_MMA && XSPLIT && it > beg) load_b(g, bcur, blo);
+        if (MODE == PATH_MMA && XSPLIT && !XS32 && it > beg) load_b(g, bcur, blo);
         if (PREFETCH && it + 1 < end)
             load_b((s + 1 == NS ? 0 : s + 1) * W + warp,
                    reinterpret_cast<uint32_t (&)[NT][8][2]>(bnxt), blo);
         const uint8_t *stage = ring + slot * SB;
         const uint8_t *wtiles = stage + warp * TILE_BYTES;
+        if (XS32) {
+            // B fragments (k = 16j + 2t + {0, 1} and + 8) of the single
+            // activation row, each f32 pair split into bf16 hi + bf16 lo
+            const float *xs = reinterpret_cast<const float *>(stage + TILES_BYTES) + warp * G + 2 * t;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 xv = *reinterpret_cast<const float2 *>(xs + 16 * j + 8 * h);
+                    const uint32_t vh = pack_bf16x2(xv.x, xv.y);
+                    bcur[0][j][h] = vh;
+                    blo[0][j][h] = pack_bf16x2(xv.x - bf16_lo_f32(vh), xv.y - bf16_hi_f32(vh));
+                }
+        }
         if (XSTAGED) {
             // Lanes of batch rows >= M read row M - 1: their MMA columns are
             // never stored, and an MMA column depends on its own B column
@@ -736,8 +754,11 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false, int RBT = RB>
 struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    static constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
     static int smem(int M)
     {
+        if (XS32)  // f32 staging as in the FMA path, MMA-sized reduction buffers
+            return NSTG * stage_bytes(PATH_FMA, 0, RBT) + CTRL_BYTES + W * RBT * 16 * 4 + RBT * 16 * 4;
         return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG, RBT);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
@@ -802,6 +823,8 @@ static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, bool small,
         if (M == 1) return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true>{});
         return two ? f(Kern<PATH_MMA, 2, 0, false>{}) : f(Kern<PATH_MMA, 1, 0, false>{});
     }
+    if (M == 1)
+        return deep ? f(Kern<PATH_MMA, 1, 0, true, 3, true>{}) : f(Kern<PATH_MMA, 1, 0, true, NSTAGE, true>{});
     return two ? f(Kern<PATH_MMA, 2, 0, true>{}) : f(Kern<PATH_MMA, 1, 0, true>{});
 }
 
@@ -813,12 +836,12 @@ size_t gemv_counter_bytes(int64_t N)
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
 {
     GemvPlan p{};
-    // AUTO: the tensor-core path for bf16/f16 activations (its unpack costs 7
-    // ALU instructions per 8 weights against 11 for the CUDA-core path, which
-    // is bound by the ALU pipe near half of HBM bandwidth); the CUDA-core path
-    // for f32 activations at M = 1 (the tensor-core path would need two MMAs
-    // per step for the hi/lo split of each activation).
-    if (path == PATH_AUTO) path = (M == 1 && xt == Q4_F32) ? PATH_FMA : PATH_MMA;
+    // AUTO: the tensor-core path (its unpack costs 7 ALU instructions per 8
+    // weights against 11 for the CUDA-core path, which is bound by the ALU
+    // pipe); f32 activations ride as bf16 hi + lo with two MMAs per word,
+    // staged as f32 with the tiles at M = 1 (measured 6-11% faster than the
+    // CUDA-core path there).
+    if (path == PATH_AUTO) path = PATH_MMA;
     p.path = path;
     const int ntiles = (N + TILE_ROWS - 1) / TILE_ROWS;
     const int NG = K / G;
@@ -843,8 +866,7 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     p.grid = static_cast<int>(T < slots ? T : slots);
     // The 3-stage ring pays off once each CTA streams many steps; with only a
     // few, the deeper first wave of requests delays every CTA's first step.
-    p.deep = !p.small && path == PATH_MMA && M == 1 && xt != Q4_F32 &&
-             T >= 8 * static_cast<int64_t>(p.grid);
+    p.deep = !p.small && path == PATH_MMA && M == 1 && T >= 8 * static_cast<int64_t>(p.grid);
     if (p.deep) {  // same CTAs per SM, or keep the 2-stage ring
         int per_sm_deep = 0;
         dispatch(path, M, xt, true, false,
