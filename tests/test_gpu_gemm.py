@@ -27,6 +27,20 @@ def test_gemm_parity(M, N, K, xdt):
         compare(y, y_ref, absdot, where=f"gemm {M}x{N}x{K} y={ydt}")
 
 
+@pytest.mark.parametrize("M", [1, 17, 32])
+def test_gemm_small_m(M):
+    """q4_gemm accepts any M >= 1; a batch far below one 256-token tile."""
+    import weight_only_int4_group_gb300 as q4
+    N, K = 384, 2048
+    W = synth.normal_rows(M + 11, K, 0, N, 0.02)
+    x, xf = x_for(torch.bfloat16, M, K, seed=M + 3)
+    _, y_ref, absdot = oracle_product(W, xf)
+    y = q4.gemm(x, q4.QWeight.from_float(dev_f32(W)), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert q4.check() == q4.OK
+    compare(y, y_ref, absdot, where=f"gemm M={M}")
+
+
 def test_gemm_outputs_untouched_beyond_bounds():
     """Ragged M and N: rows and columns past the matrix are not written."""
     import weight_only_int4_group_gb300 as q4
