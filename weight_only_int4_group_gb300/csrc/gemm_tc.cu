@@ -470,13 +470,13 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
     auto kern = f16 ? (yf16 ? k_gemm<true, true> : k_gemm<true, false>)
                     : (yf16 ? k_gemm<false, true> : k_gemm<false, false>);
     const int variant = (f16 ? 2 : 0) + (yf16 ? 1 : 0);
-    static bool configured[4][64] = {};
+    static std::atomic<bool> configured[4][64];  // concurrent first calls may both set it
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[variant][dev]) {
+    if (dev < 0 || dev >= 64 || !configured[variant][dev].load(std::memory_order_relaxed)) {
         *cerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
-        configured[variant][dev] = true;
+        if (dev >= 0 && dev < 64) configured[variant][dev].store(true, std::memory_order_relaxed);
     }
     kern<<<grid, THREADS, SMEM_ALLOC, s>>>(tmx, a);
     *cerr = cudaGetLastError();

@@ -763,25 +763,28 @@ struct Kern {
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
     {
-        static int cached[64][17] = {};
-        static bool attr[64] = {};
+        // per-device caches; concurrent first calls may both fill them (the
+        // same values), so relaxed atomics suffice
+        static std::atomic<int> cached[64][17];
+        static std::atomic<bool> attr[64];
         if (dev < 0 || dev >= 64 || M < 1 || M > 16) return cudaErrorInvalidValue;
-        if (cached[dev][M] > 0) {
-            *blocks_per_sm = cached[dev][M];
+        const int known = cached[dev][M].load(std::memory_order_relaxed);
+        if (known > 0) {
+            *blocks_per_sm = known;
             return cudaSuccess;
         }
         auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT>;
-        if (!attr[dev]) {
+        if (!attr[dev].load(std::memory_order_relaxed)) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem(NSTG == NSTAGE ? 16 : 1));
             if (e != cudaSuccess) return e;
-            attr[dev] = true;
+            attr[dev].store(true, std::memory_order_relaxed);
         }
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, THREADS, smem(M));
         if (e != cudaSuccess) return e;
         if (n < 1) n = 1;
-        cached[dev][M] = n;
+        cached[dev][M].store(n, std::memory_order_relaxed);
         *blocks_per_sm = n;
         return cudaSuccess;
     }
