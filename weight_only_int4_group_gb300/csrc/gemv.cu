@@ -53,6 +53,9 @@
 //     lane loads its B fragments from L2 one step ahead.  The group sums of the
 //     activations come from one extra MMA per k-step with an all-ones A
 //     operand.  Per group, y += scale * (D - (offset + zero) * sum x).
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
 
 namespace q4 {
@@ -836,7 +839,50 @@ size_t gemv_counter_bytes(int64_t N)
     return ((static_cast<size_t>((N + 31) / 32) * sizeof(unsigned int) + 255) / 256) * 256;
 }
 
+static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
+
+// Plans depend only on (device, shape, activation type, path); a decode loop
+// asks for the same few again and again, so they are kept (a small map,
+// cleared if it ever grows large).
 GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
+{
+    struct Key {
+        int dev, M, N, K, xt, path, sms;
+        bool operator==(const Key &o) const
+        {
+            return dev == o.dev && M == o.M && N == o.N && K == o.K && xt == o.xt &&
+                   path == o.path && sms == o.sms;
+        }
+    };
+    struct Hash {
+        size_t operator()(const Key &k) const
+        {
+            uint64_t h = 1469598103934665603ull;
+            for (int v : {k.dev, k.M, k.N, k.K, k.xt, k.path, k.sms})
+                h = (h ^ static_cast<uint32_t>(v)) * 1099511628211ull;
+            return static_cast<size_t>(h);
+        }
+    };
+    static std::mutex mu;
+    static std::unordered_map<Key, GemvPlan, Hash> plans;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const Key key{dev, M, N, K, static_cast<int>(xt), path, sm_count};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = plans.find(key);
+        if (it != plans.end()) return it->second;
+    }
+    const GemvPlan p = make_plan(M, N, K, xt, path, sm_count);
+    if (p.grid > 0) {  // a plan whose kernel configuration failed is not kept
+        std::lock_guard<std::mutex> lock(mu);
+        if (plans.size() > 4096) plans.clear();
+        plans.emplace(key, p);
+    }
+    return p;
+}
+
+static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
 {
     GemvPlan p{};
     // AUTO: the tensor-core path (its unpack costs 7 ALU instructions per 8
@@ -851,17 +897,17 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     const int NS = (NG + W - 1) / W;
     int dev = 0, per_sm = 1;
     cudaGetDevice(&dev);
-    dispatch(path, M, xt, false, false,
-             [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    cudaError_t cfg = dispatch(path, M, xt, false, false,
+                               [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
     // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 8: use
     // 2-tile ones, so that steps are short and plentiful (measured faster
     // there; at M = 1 the longer steps win).
     const int64_t T8 = static_cast<int64_t>((ntiles + RB - 1) / RB) * NS;
     p.small = T8 < 4 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 2 &&
               M <= 8 && xt != Q4_F32;
-    if (p.small)
-        dispatch(path, M, xt, false, true,
-                 [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
+    if (p.small && cfg == cudaSuccess)
+        cfg = dispatch(path, M, xt, false, true,
+                       [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
     p.rb = p.small ? RB_SMALL : RB;
     p.nrb = (ntiles + p.rb - 1) / p.rb;
     const int64_t T = static_cast<int64_t>(p.nrb) * NS;
@@ -893,6 +939,7 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     p.workspace = maxc > 1 ? gemv_counter_bytes(N) + static_cast<size_t>(p.nrb) * maxc * p.rb * 16 *
                                                          static_cast<size_t>(M) * sizeof(float)
                            : 0;
+    if (cfg != cudaSuccess) p.grid = 0;  // the launch then fails and reports it
     return p;
 }
 
