@@ -197,12 +197,18 @@ class Decode70B:
         self.weights_bytes = layers * sum(q4.weight_bytes(N, K) for _, N, K in LAYER_SHAPES)
         self.launches_per_step = layers * len(LAYER_SHAPES)
 
+    def views(self):
+        """Per-call (x, y) views into the step's activation and output buffers,
+        made once (a caller holds its tensors across steps)."""
+        if not hasattr(self, "_views"):
+            self._views = [[(self.x[self.x_off[l][i]:self.x_off[l][i] + self.M * K].view(self.M, K),
+                             self.y[self.y_off[l][i]:self.y_off[l][i] + self.M * N].view(self.M, N))
+                            for i, (_, N, K) in enumerate(LAYER_SHAPES)] for l in range(self.L)]
+        return self._views
+
     def gemv(self, l: int, i: int, path=0):
-        _, N, K = LAYER_SHAPES[i]
-        q4 = self.q4
-        x = self.x[self.x_off[l][i]:self.x_off[l][i] + self.M * K].view(self.M, K)
-        y = self.y[self.y_off[l][i]:self.y_off[l][i] + self.M * N].view(self.M, N)
-        q4.gemv(x, self.qw[l][i], out=y, ws=self.ws[N], path=path)
+        x, y = self.views()[l][i]
+        self.q4.gemv(x, self.qw[l][i], out=y, ws=self.ws[LAYER_SHAPES[i][1]], path=path)
 
     def step(self, path=0):
         for l in range(self.L):

@@ -36,7 +36,7 @@ namespace gm {
 
 constexpr int BM = 256, SUB = 128, BN = 128, BK = 64;
 constexpr int NA = 4;   // activation stages (latency of the L2 reads of X)
-constexpr int NBS = 3;  // dequantized-weight stages
+constexpr int NBS = 4;  // dequantized-weight stages
 constexpr int NC = 2;   // packed-code stages (one group = two k stages)
 constexpr int RT = BN / TILE_ROWS;         // 8 row tiles per weight tile
 constexpr int A_BOX = SUB * BK * 2;        // 16384: one 128 x 64 activation box

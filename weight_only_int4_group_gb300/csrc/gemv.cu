@@ -816,8 +816,7 @@ static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, bool small,
         if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL>{});
         return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL>{});
     }
-    // deep: M = 1 with 16-bit activations, where a 3-stage ring still fits
-    // two CTAs per SM
+    // deep: M = 1, where a 3-stage ring still fits two CTAs per SM
     const bool two = M > 8;
     if (xt == Q4_F16) {
         if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3, true>{});
@@ -920,9 +919,9 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
         const int64_t per = (T + slots - 1) / slots;
         p.grid = static_cast<int>((T + per - 1) / per);
     }
-    // The 3-stage ring pays off once each CTA streams many steps; with only a
-    // few, the deeper first wave of requests delays every CTA's first step.
-    p.deep = !p.small && path == PATH_MMA && M == 1 && T >= 8 * static_cast<int64_t>(p.grid);
+    // The 3-stage ring pays off once each CTA streams 5 or more steps; with
+    // fewer, the deeper first wave of requests delays every CTA's first step.
+    p.deep = !p.small && path == PATH_MMA && M == 1 && T >= 5 * static_cast<int64_t>(p.grid);
     if (p.deep) {  // same CTAs per SM, or keep the 2-stage ring
         int per_sm_deep = 0;
         dispatch(path, M, xt, true, false,
