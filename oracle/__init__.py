@@ -1,11 +1,14 @@
-"""CPU oracle for asymmetric group-128 INT4 quantization and the W4A16 product.
+"""CPU oracle for group-128 INT4 quantization (asymmetric and symmetric) and the
+W4A16 product.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only users.  The product library never imports it,
 and it never imports the product library.
 
 The arithmetic lives in plain C (``oq4.c``), written from the page "Weight
-quantization" (tirogla.com), sections "How it works" and "Code".  This module
+quantization" (tirogla.com), sections "How it works" and "Code"; the
+symmetric scheme from the page "Quantization" (hritesh-sonawane.github.io
+notes), sections "How it really works" and "Code".  This module
 only compiles it with gcc and marshals numpy arrays through ctypes.  ctypes
 releases the GIL during each call, so callers may run disjoint row ranges on
 several Python threads.
@@ -52,6 +55,8 @@ class Oracle:
         lib = ctypes.CDLL(path)
         lib.oq4_quantize_g.argtypes = [_P, _I, _I, _I, _P, _P, _P]
         lib.oq4_quantize_g.restype = ctypes.c_int
+        lib.oq4_quantize_sym_g.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+        lib.oq4_quantize_sym_g.restype = ctypes.c_int
         lib.oq4_dequant_g.argtypes = [_P, _P, _P, _I, _I, _I, _P]
         lib.oq4_dequant_g.restype = None
         lib.oq4_dot_naive.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P]
@@ -66,8 +71,10 @@ class Oracle:
         self.mutant = lib.oq4_mutant()
 
     # -- quantize / dequantize ------------------------------------------------
-    def quantize(self, w: np.ndarray, group: int = G):
-        """w: f32 [N][K] -> (packed u8 [N][K/2], scale f32 [N][K/G], zero u8 [N][K/G])."""
+    def quantize(self, w: np.ndarray, group: int = G, symmetric: bool = False):
+        """w: f32 [N][K] -> (packed u8 [N][K/2], scale f32 [N][K/G], zero u8 [N][K/G]).
+
+        ``symmetric`` selects the absmax/7 scheme (codes q + 8, zero 8)."""
         w = np.ascontiguousarray(w, dtype=np.float32)
         if w.ndim == 1:
             w = w[None, :]
@@ -75,8 +82,9 @@ class Oracle:
         packed = np.zeros((N, K // 2), np.uint8)
         scale = np.zeros((N, K // group), np.float32)
         zero = np.zeros((N, K // group), np.uint8)
-        rc = self.lib.oq4_quantize_g(w.ctypes.data, N, K, group, packed.ctypes.data,
-                                     scale.ctypes.data, zero.ctypes.data)
+        fn = self.lib.oq4_quantize_sym_g if symmetric else self.lib.oq4_quantize_g
+        rc = fn(w.ctypes.data, N, K, group, packed.ctypes.data, scale.ctypes.data,
+                zero.ctypes.data)
         if rc != 0:
             raise ValueError(f"oracle quantize rejected shape {N}x{K} with G={group}")
         return packed, scale, zero

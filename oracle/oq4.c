@@ -124,6 +124,65 @@ int oq4_quantize(const float *w, int64_t N, int64_t K,
     return oq4_quantize_g(w, N, K, OQ4_G, packed, scale, zero);
 }
 
+/* Symmetric variant (page "Quantization", hritesh-sonawane.github.io notes,
+ * section "How it really works", "The mechanics: scale, round, clamp", and
+ * its "Code" section, function int_quant; page "LLM Quantization Architecture
+ * in Depth", the group-wise symmetric listing):
+ *   s = max|w| / 7, or 1 when that is 0     (the "or 1.0" of int_quant)
+ *   q = clamp(round(w / s), -8, 7)          (round = ties to even, as both
+ *                                            pages' round() does)
+ *   w_hat = q * s
+ * Stored in the same containers as the asymmetric scheme: code q + 8 in the
+ * nibble and zero = 8, so that (code - zero) * s == q * s exactly. */
+static float round_sym(float v)
+{
+#if OQ4_MUTANT == 12
+    return roundf(v);
+#else
+    return rintf(v);
+#endif
+}
+
+int oq4_quantize_sym_g(const float *w, int64_t N, int64_t K, int64_t G,
+                       uint8_t *packed, float *scale, uint8_t *zero)
+{
+    if (G <= 0 || K % G != 0 || ((N * K) & 1)) return -1;
+    memset(packed, 0, (size_t)(N * K / 2));
+    const int64_t ngroups = N * K / G;
+    for (int64_t gi = 0; gi < ngroups; ++gi) {
+        const float *grp = w + gi * G;
+        /* 1. largest magnitude of the group */
+        float amax = 0.0f;
+        for (int64_t j = 0; j < G; ++j) amax = fmaxf(amax, fabsf(grp[j]));
+        /* 2. scale = max|w| / (2^(b-1) - 1), 1 when the quotient is 0 */
+#if OQ4_MUTANT == 13
+        float s = amax / 8.0f;
+#else
+        float s = amax / 7.0f;
+#endif
+        if (s == 0.0f) s = 1.0f;
+        scale[gi] = s;
+#if OQ4_MUTANT == 14
+        const float off = 7.0f;
+#else
+        const float off = 8.0f;
+#endif
+        zero[gi] = 8;
+        /* 3. q = clamp(round(w / s), -8, 7), stored as q + 8 */
+        for (int64_t j = 0; j < G; ++j) {
+            float qf = clampf(round_sym(grp[j] / s), -8.0f, 7.0f);
+            put_code(packed, gi * G + j, (uint8_t)(qf + off));
+        }
+    }
+    return 0;
+}
+
+int oq4_quantize_sym(const float *w, int64_t N, int64_t K,
+                     uint8_t *packed, float *scale, uint8_t *zero)
+{
+    return oq4_quantize_sym_g(w, N, K, OQ4_G, packed, scale, zero);
+}
+
 /* w_hat = (q - zero) * scale  ("How it works", last formula).  Both factors
  * are exact in double, and so is their product (4-bit x 24-bit). */
 static double what_at(const uint8_t *packed, const float *scale, const uint8_t *zero,

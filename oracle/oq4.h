@@ -1,6 +1,7 @@
 /*
- * oq4.h -- CPU oracle for asymmetric group-wise INT4 weight quantization and
- * the weight-only (W4A16) matrix-vector product.
+ * oq4.h -- CPU oracle for group-wise INT4 weight quantization (asymmetric,
+ * and the symmetric variant) and the weight-only (W4A16) matrix-vector
+ * product.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
  * load or execute this code: only the test suite, the smoke check and the
@@ -42,6 +43,18 @@ int oq4_quantize_g(const float *w, int64_t N, int64_t K, int64_t G,
 /* Same with G = 128. */
 int oq4_quantize(const float *w, int64_t N, int64_t K,
                  uint8_t *packed, float *scale, uint8_t *zero);
+
+/* Symmetric round-to-nearest with group size G: s = max|w|/7 (1 when that
+ * quotient is 0), q = clamp(rint(w/s), -8, 7) with ties to even, stored as
+ * code q + 8 with zero = 8 in the same containers, so the dequantization and
+ * products below serve both schemes.  Source: page "Quantization"
+ * (hritesh-sonawane.github.io notes), "How it really works" and "Code"
+ * (int_quant); page "LLM Quantization Architecture in Depth", the group-wise
+ * symmetric listing.  Returns 0, or -1 on a bad shape (as above). */
+int oq4_quantize_sym_g(const float *w, int64_t N, int64_t K, int64_t G,
+                       uint8_t *packed, float *scale, uint8_t *zero);
+int oq4_quantize_sym(const float *w, int64_t N, int64_t K,
+                     uint8_t *packed, float *scale, uint8_t *zero);
 
 /* w_hat[n][k] = (q - zero) * scale, exactly, in double. */
 void oq4_dequant_g(const uint8_t *packed, const float *scale, const uint8_t *zero,

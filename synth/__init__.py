@@ -13,6 +13,9 @@ Workload recipes (shapes and distributions of the pages' workloads):
   * ``normal_rows`` / ``dev_normal_f32``: W ~ N(0, sigma) per element by flat
     index, optional outlier columns multiplied by a factor.
   * ``normal_bf16`` / ``dev_normal_bf16``: activations ~ N(0,1) rounded to bf16.
+  * ``row_scaled_outliers``: the 256x1024 matrix with per-row spreads and
+    eight outliers of the page "Quantization" (hritesh-sonawane.github.io
+    notes), section "Code" (Python's Mersenne Twister).
 """
 from __future__ import annotations
 
@@ -119,6 +122,31 @@ def xorshift_matrix(N: int, K: int):
     r, _ = xorshift_stream(N * K + K)
     W = (np.float32(0.02) * r[:N * K]).astype(np.float32).reshape(N, K)
     return W, r[N * K:].copy()
+
+
+def row_scaled_outliers(rows: int = 256, cols: int = 1024, seed: int = 11,
+                        n_outliers: int = 8, magnitude: float = 0.6) -> np.ndarray:
+    """The synthetic matrix of the page "Quantization" (hritesh-sonawane.github.io
+    notes), section "Code": each row draws its own spread 0.02*exp(N(0, 0.5))
+    and then ``cols`` values N(0, spread); afterwards ``n_outliers`` entries
+    become +-``magnitude``, each drawing its sign, then its row, then its
+    column.  Draws come from Python's own generator (``random.Random``,
+    Mersenne Twister, its ``gauss``) in exactly that order, so the error table
+    the page prints for this matrix applies to it.  Returns f64 [rows][cols]."""
+    import math
+    import random
+
+    gen = random.Random(seed)
+    out = np.empty((rows, cols), np.float64)
+    for r in range(rows):
+        spread = 0.02 * math.exp(gen.gauss(0.0, 0.5))
+        out[r, :] = [gen.gauss(0.0, spread) for _c in range(cols)]
+    for _i in range(n_outliers):
+        sign = gen.choice((-1, 1))
+        r = gen.randrange(rows)
+        c = gen.randrange(cols)
+        out[r, c] = sign * magnitude
+    return out
 
 
 def uniform(seed: int, start: int, count: int, scale: float = 1.0) -> np.ndarray:

@@ -264,6 +264,92 @@ def pin_matrix_bound(o, N: int = 1024, K: int = 4096):
     assert (np.abs(y[0] - exact) < 0.02 * mag).all()
 
 
+
+# --------------------------------------------------------- symmetric variant
+# Page cited: "Quantization" (hritesh-sonawane.github.io notes), sections
+# "How it really works" (scale = max|x| / (2^(b-1) - 1), q = clamp(round(x /
+# scale)), x_hat = q * scale) and "Code" (int_quant and its printed table).
+
+def _sym_codes(o, W, group=128):
+    W = np.atleast_2d(np.asarray(W, np.float32))
+    packed, scale, zero = o.quantize(W, group=group, symmetric=True)
+    c = _codes(packed, W.size).reshape(W.shape)
+    return c, scale, zero
+
+
+def pin_sym_page_table(o):
+    """The INT4 rows of the page's printed error table (per tensor, per
+    channel, group 128, group 32), reproduced on the page's own synthetic
+    matrix to the printed precision."""
+    gold = read_golden("page_int4_error_table.txt")
+    R, C = gold["rows"], gold["cols"]
+    w = synth.row_scaled_outliers(R, C, gold["seed"])
+    wf = w.astype(np.float32)
+    for key, shape, group in (("tensor", (1, R * C), R * C), ("channel", (R, C), C),
+                              ("g128", (R, C), 128), ("g32", (R, C), 32)):
+        packed, scale, zero = o.quantize(wf.reshape(shape), group=group, symmetric=True)
+        wh = o.dequant(packed, scale, zero, shape[0], shape[1], group=group).reshape(R, C)
+        sig = float((w * w).sum())
+        err = float(((w - wh) ** 2).sum())
+        assert f"{10 * np.log10(sig / err):.1f}" == f"{gold[key + '_sqnr_db']:.1f}", key
+        assert f"{100 * np.sqrt(err / sig):.2f}" == f"{gold[key + '_rel_pct']:.2f}", key
+
+
+def pin_sym_ties_to_even(o):
+    """With max|w| = 7 the scale is exactly 1, so w / scale = w: the halves
+    2.5, -2.5, 3.5, -0.5, 6.5 round to the even neighbours 2, -2, 4, 0, 6
+    (Python's round and torch.round, which both pages use); stored codes are
+    q + 8 with zero 8."""
+    v = np.zeros(128, np.float32)
+    v[0] = 7.0
+    v[1:6] = [2.5, -2.5, 3.5, -0.5, 6.5]
+    v[6:10] = [1.0, -7.0, -3.0, 0.25]
+    c, scale, zero = _sym_codes(o, v)
+    assert scale[0, 0] == np.float32(1.0) and zero[0, 0] == 8
+    assert list(c[0, :10] - 8) == [7, 2, -2, 4, 0, 6, 1, -7, -3, 0]
+
+
+def pin_sym_special_groups(o):
+    """Closed forms: an all-zero group has scale 1 (the page's "or 1.0") and
+    codes 8; a constant group c has scale |c|/7 and q = +-7; the largest
+    magnitude always maps to +-7; a group whose max|w|/7 underflows to 0 gets
+    scale 1 as well."""
+    tiny = np.float32(np.ldexp(1.0, -149))
+    rng = np.random.default_rng(21)
+    mixed = rng.normal(0, 0.02, 128).astype(np.float32)
+    W = np.stack([np.zeros(128, np.float32), np.full(128, 0.7, np.float32),
+                  np.full(128, -0.3, np.float32), mixed, np.full(128, tiny, np.float32)])
+    c, scale, zero = _sym_codes(o, W)
+    q = c.astype(np.int64) - 8
+    assert (zero == 8).all()
+    assert scale[0, 0] == 1.0 and (q[0] == 0).all()
+    assert scale[1, 0] == np.float32(0.7) / np.float32(7.0) and (q[1] == 7).all()
+    assert scale[2, 0] == np.float32(0.3) / np.float32(7.0) and (q[2] == -7).all()
+    i = int(np.argmax(np.abs(mixed)))
+    assert q[3, i] == (7 if mixed[i] > 0 else -7)
+    assert abs(7.0 * float(scale[3, 0]) - abs(float(mixed[i]))) <= 2 ** -21 * abs(float(mixed[i]))
+    assert scale[4, 0] == 1.0 and (q[4] == 0).all()
+
+
+def pin_sym_half_step_and_nearest(o):
+    """|w - w_hat| <= scale/2 for every element (no clamping occurs since
+    |w / scale| <= 7), w == 0 reconstructs to 0, and each code is a nearest
+    point of the grid {-8..7} * scale up to the f32 rounding of w / scale."""
+    rng = np.random.default_rng(23)
+    W = _random_groups(rng)
+    N, K = W.shape
+    c, scale, zero = _sym_codes(o, W)
+    wh = o.dequant(*o.quantize(W, symmetric=True), N, K)
+    s = np.repeat(scale.astype(np.float64), 128, axis=1)
+    Wd = W.astype(np.float64)
+    assert (np.abs(Wd - wh) <= 0.5 * s * (1 + 2 ** -16) + 16 * np.abs(Wd) * 2.0 ** -24).all()
+    assert (wh[W == 0] == 0.0).all()
+    grid = np.arange(-8, 8, dtype=np.float64)
+    dist = np.abs(Wd[:, :, None] - grid[None, None, :] * s[:, :, None])
+    chosen = np.take_along_axis(dist, (c.astype(np.int64))[:, :, None], axis=2)[:, :, 0]
+    assert (chosen <= dist.min(axis=2) + 2.0 ** -20 * s + 2.0 ** -22 * np.abs(Wd)).all()
+
+
 ALL_PINS = [
     pin_page_program,
     pin_closed_form_integer_group,
@@ -277,4 +363,8 @@ ALL_PINS = [
     pin_factored_identity,
     pin_xsum,
     pin_matrix_bound,
+    pin_sym_page_table,
+    pin_sym_ties_to_even,
+    pin_sym_special_groups,
+    pin_sym_half_step_and_nearest,
 ]
