@@ -680,7 +680,8 @@ def extra_rows(q4, torch, work, pk) -> dict:
     del g, xg, yg
     torch.cuda.empty_cache()
 
-    # quantizer: HBM-bound, 4 B read + 0.539 B written per weight
+    # quantizers (asymmetric, symmetric): HBM-bound, 4 B read + 0.539 B
+    # written per weight
     N, K = 57344, 8192
     import synth
     w = torch.empty((N, K), dtype=torch.float32, device=dev)
@@ -690,15 +691,17 @@ def extra_rows(q4, torch, work, pk) -> dict:
     zero = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
     lib = q4.lib()
 
-    def qrun():
-        lib.q4_quantize(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(), zero.data_ptr(),
-                        torch.cuda.current_stream().cuda_stream)
-    g = graph_of(torch, qrun)
-    t = time_graph(torch, g, reps=10)
     b = 4 * N * K + N * K // 2 + 5 * N * K // 128
-    rows["quantize"] = {"shape": f"{N}x{K} f32", "ms": round(t * 1e3, 3),
-                        "GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
-    del w, packed, scale, zero, g
+    for key, fn in (("quantize", lib.q4_quantize), ("quantize_sym", lib.q4_quantize_sym)):
+        def qrun(fn=fn):
+            fn(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(), zero.data_ptr(),
+               torch.cuda.current_stream().cuda_stream)
+        g = graph_of(torch, qrun)
+        t = time_graph(torch, g, reps=10)
+        rows[key] = {"shape": f"{N}x{K} f32", "ms": round(t * 1e3, 3),
+                     "GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4)}
+        del g
+    del w, packed, scale, zero
     torch.cuda.empty_cache()
     return rows
 

@@ -81,6 +81,19 @@ typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
 q4_status q4_quantize(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
                       uint8_t *zero, q4_stream_t stream);
 
+/*
+ * Symmetric variant (page "Quantization", hritesh-sonawane.github.io notes,
+ * sections "How it really works" and "Code", int_quant; page "LLM
+ * Quantization Architecture in Depth", the group-wise symmetric listing):
+ * per group of 128, scale = max|w| / 7 in IEEE f32 (1 when that quotient is
+ * 0) and q = clamp(round(w / scale), -8, 7) with ties to even.  Writes the
+ * same canonical arrays as q4_quantize: code q + 8 in each nibble and zero 8,
+ * so (code - zero) * scale = q * scale and q4_repack, q4_gemv and q4_gemm
+ * serve it unchanged.  Same arguments and errors as q4_quantize.
+ */
+q4_status q4_quantize_sym(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                          uint8_t *zero, q4_stream_t stream);
+
 /* Bytes of the tiled kernel layout for an N x K matrix: ceil(N/16) row tiles
  * times K/128 groups times Q4_TILE_BYTES.  0 for invalid sizes. */
 size_t q4_weight_bytes(int64_t N, int64_t K);

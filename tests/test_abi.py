@@ -27,7 +27,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("q4_quantize", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemm",
+    for must in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemm",
                  "q4_check", "q4_status_str", "q4_weight_bytes", "q4_gemv_workspace_bytes"):
         assert must in names
 
@@ -72,6 +72,11 @@ def test_host_side_argument_errors(lib):
     assert lib.q4_quantize(fake, 0, 128, fake, fake, fake, None) == 1
     # misaligned input
     assert lib.q4_quantize(fake + 4, 4, 128, fake, fake, fake, None) == 3
+    # the symmetric quantizer shares the checks
+    lib.q4_quantize_sym.argtypes = [P, I, I, P, P, P, P]
+    assert lib.q4_quantize_sym(None, 4, 128, fake, fake, fake, None) == 1
+    assert lib.q4_quantize_sym(fake, 4, 100, fake, fake, fake, None) == 1
+    assert lib.q4_quantize_sym(fake + 4, 4, 128, fake, fake, fake, None) == 3
     assert lib.q4_repack(fake, fake, fake, 4, 128, fake + 8, None) == 3
     # GEMV: M outside [1, 16] is unsupported, bad dtype unsupported, misaligned
     assert lib.q4_gemv(fake, 1, 0, 64, 128, fake, fake, 0, None, 0, None) == 2

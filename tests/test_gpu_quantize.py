@@ -33,10 +33,16 @@ def _edge_matrix(N, K, seed):
         W[9, 2::128] = 0.0
         W[10][rng.random(K) < 0.2] = 0.0                 # exact zeros
         W[11] = -0.0                                     # negative zeros
+    if N >= 14:
+        W[12] = np.float32(np.ldexp(3.0, -149))          # subnormal weights, subnormal scale
+        W[12, 1::5] = np.float32(np.ldexp(-7.0, -149))
+        W[13] = np.float32(np.ldexp(40.0, -149))         # one-signed subnormal group
+        # (a range below 15 x the smallest subnormal would make the scale 0:
+        # outside the contract, like non-finite weights)
     return W
 
 
-SHAPES = [(1, 128), (2, 256), (12, 128), (200, 1024), (33, 4096), (16, 11008)]
+SHAPES = [(1, 128), (2, 256), (12, 128), (14, 256), (200, 1024), (33, 4096), (16, 11008)]
 
 
 @pytest.mark.parametrize("N,K", SHAPES)

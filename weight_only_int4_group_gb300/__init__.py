@@ -5,8 +5,8 @@ PyTorch is used for device memory and the current CUDA stream.  Importing
 this package fails loudly when libq4.so has not been built; there is no
 fallback of any kind.
 
-Names follow include/q4.h: quantize, repack, unpack, xsum, gemv, gemm,
-check, weight_bytes, gemv_workspace_bytes.
+Names follow include/q4.h: quantize, quantize_sym, repack, unpack, xsum,
+gemv, gemm, check, weight_bytes, gemv_workspace_bytes.
 """
 from __future__ import annotations
 
@@ -46,6 +46,7 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I, Z, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
     lib.q4_quantize.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_quantize_sym.argtypes = [P, I, I, P, P, P, P]
     lib.q4_weight_bytes.argtypes = [I, I]
     lib.q4_weight_bytes.restype = Z
     lib.q4_repack.argtypes = [P, P, P, I, I, P, P]
@@ -61,7 +62,7 @@ def _load():
     lib.q4_status_str.argtypes = [S]
     lib.q4_status_str.restype = ctypes.c_char_p
     lib.q4_last_cuda_error.restype = ctypes.c_char_p
-    for f in ("q4_quantize", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemv_path",
+    for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemv_path",
               "q4_gemv_timeout_selftest", "q4_gemm", "q4_check"):
         getattr(lib, f).restype = S
     return lib
@@ -102,8 +103,10 @@ def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(_lib.q4_gemv_workspace_bytes(M, N, K))
 
 
-def quantize(w: torch.Tensor, stream=None):
-    """w f32 [N][K] (cuda) -> (packed u8 [N][K/2], scale f32 [N][K/128], zero u8 [N][K/128])."""
+def quantize(w: torch.Tensor, stream=None, symmetric: bool = False):
+    """w f32 [N][K] (cuda) -> (packed u8 [N][K/2], scale f32 [N][K/128], zero u8 [N][K/128]).
+
+    ``symmetric`` calls q4_quantize_sym (max|w|/7 scales, zero 8)."""
     _cuda(w, "w")
     if w.dtype != torch.float32 or w.dim() != 2:
         raise ValueError("w must be a 2-D float32 tensor")
@@ -111,9 +114,16 @@ def quantize(w: torch.Tensor, stream=None):
     packed = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
     scale = torch.empty((N, max(K // GROUP, 1)), dtype=torch.float32, device=w.device)
     zero = torch.empty((N, max(K // GROUP, 1)), dtype=torch.uint8, device=w.device)
-    _ok(_lib.q4_quantize(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(),
-                         zero.data_ptr(), _stream(stream)), "q4_quantize")
+    fn, name = (_lib.q4_quantize_sym, "q4_quantize_sym") if symmetric else \
+        (_lib.q4_quantize, "q4_quantize")
+    _ok(fn(w.data_ptr(), N, K, packed.data_ptr(), scale.data_ptr(), zero.data_ptr(),
+           _stream(stream)), name)
     return packed, scale, zero
+
+
+def quantize_sym(w: torch.Tensor, stream=None):
+    """Symmetric group-128 quantization (q4_quantize_sym); same outputs as quantize."""
+    return quantize(w, stream, symmetric=True)
 
 
 def repack(packed: torch.Tensor, scale: torch.Tensor, zero: torch.Tensor, N: int, K: int,
@@ -158,9 +168,9 @@ class QWeight:
     K: int
 
     @classmethod
-    def from_float(cls, w: torch.Tensor, stream=None) -> "QWeight":
+    def from_float(cls, w: torch.Tensor, stream=None, symmetric: bool = False) -> "QWeight":
         N, K = w.shape
-        packed, scale, zero = quantize(w, stream)
+        packed, scale, zero = quantize(w, stream, symmetric=symmetric)
         return cls(repack(packed, scale, zero, N, K, stream=stream), N, K)
 
 

@@ -109,14 +109,26 @@ using namespace q4;
 
 extern "C" {
 
-q4_status q4_quantize(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                      uint8_t *zero, q4_stream_t stream)
+static q4_status quantize_common(const float *w, int64_t N, int64_t K, uint8_t *packed,
+                                 float *scale, uint8_t *zero, bool symmetric, q4_stream_t stream)
 {
     if (!w || !packed || !scale || !zero || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(w)) return Q4_ERR_MISALIGNED;
-    const cudaError_t e =
-        quantize_launch(w, N, K, packed, scale, zero, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = quantize_launch(w, N, K, packed, scale, zero, symmetric,
+                                          reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
+}
+
+q4_status q4_quantize(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                      uint8_t *zero, q4_stream_t stream)
+{
+    return quantize_common(w, N, K, packed, scale, zero, false, stream);
+}
+
+q4_status q4_quantize_sym(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
+                          uint8_t *zero, q4_stream_t stream)
+{
+    return quantize_common(w, N, K, packed, scale, zero, true, stream);
 }
 
 size_t q4_weight_bytes(int64_t N, int64_t K)

@@ -240,7 +240,7 @@ size_t gemv_counter_bytes(int64_t N);
 cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                            uint8_t *zero, cudaStream_t s);
+                            uint8_t *zero, bool symmetric, cudaStream_t s);
 cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
                           int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
 cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,

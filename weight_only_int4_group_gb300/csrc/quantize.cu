@@ -7,22 +7,46 @@
 // after rounding, low nibble = even index.  This file is compiled with
 // --fmad=false and every rounding step uses an explicit _rn intrinsic, so the
 // codes, scales and zeros are bit-identical to the page's f32 arithmetic.
+//
+// The symmetric variant follows the page "Quantization" (hritesh-sonawane.
+// github.io notes), sections "How it really works" and "Code" (int_quant):
+// scale = max|w| / 7 (1 when that quotient is 0), q = clamp(round(w / scale),
+// -8, 7) with ties to even, stored as code q + 8 with zero 8 in the same
+// canonical arrays.
 #include "common.cuh"
 
 namespace q4 {
 
-// Warp-wide minimum / maximum of one f32 per lane (exact selections).
+// Warp-wide minimum / maximum of one finite f32 per lane, exact for every
+// finite value (subnormals included): the reduction runs on integer keys whose
+// signed order is the float order (positive floats keep their bits, negative
+// ones flip their magnitude bits; the map is its own inverse).
+__device__ __forceinline__ int order_key(float v)
+{
+    const int b = __float_as_int(v);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
 __device__ __forceinline__ float warp_min(float v)
 {
-    float r;
-    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
+    int r;
+    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(order_key(v)));
+    return __int_as_float(r ^ ((r >> 31) & 0x7fffffff));
 }
 __device__ __forceinline__ float warp_max(float v)
 {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
+    int r;
+    asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(order_key(v)));
+    return __int_as_float(r ^ ((r >> 31) & 0x7fffffff));
+}
+// Warp-wide maximum of one |w| per lane: for non-negative floats the bit
+// patterns are ordered like the values.
+__device__ __forceinline__ float warp_absmax(float a)
+{
+    uint32_t r;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;"
+                 : "=r"(r)
+                 : "r"(__float_as_uint(a) & 0x7fffffffu));
+    return __uint_as_float(r);
 }
 
 // Code of one weight: clamp(round(w / s) + z, 0, 15) with the quotient of
@@ -48,6 +72,24 @@ __device__ __forceinline__ int code_of(float w, float s, float r, int z)
     return q < 0 ? 0 : (q > 15 ? 15 : q);
 }
 
+// Symmetric code: clamp(rint(w / s), -8, 7) + 8 with the IEEE f32 quotient
+// and ties to even, for |w / s| <= 16.  Same reciprocal shortcut and
+// fallback as code_of: away from a tie the rounded product names the
+// quotient's integer under any tie rule.
+__device__ __forceinline__ int code_sym(float w, float s, float r)
+{
+    const float qa = __fmul_rn(w, r);
+    const float t = __fadd_rn(qa, 12582912.0f);
+    const float rem = __fsub_rn(qa, __fsub_rn(t, 12582912.0f));
+    int q;
+    if (fabsf(rem) < 0.5f - 0x1p-16f)  // false for NaN
+        q = __float_as_int(t) - 0x4B400000;
+    else
+        q = static_cast<int>(rintf(__fdiv_rn(w, s)));
+    q = q < -8 ? -8 : (q > 7 ? 7 : q);
+    return q + 8;
+}
+
 // One warp per group of 128 weights: each lane holds 4 consecutive weights
 // (one 16-byte load), warp-wide min/max (exact, order-free), then every lane
 // quantizes its 4 weights and stores 2 packed bytes.  A warp takes GPW groups
@@ -55,6 +97,7 @@ __device__ __forceinline__ int code_of(float w, float s, float r, int z)
 // in flight to keep HBM busy) and computing their scales in one go.
 constexpr int GPW = 4;
 
+template <bool SYM>
 __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, int64_t ngroups,
                                                   uint8_t *__restrict__ packed,
                                                   float *__restrict__ scale,
@@ -71,22 +114,37 @@ __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, i
                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         // group ranges; then lane u (< GPW) computes group u's scale, zero
         // and reciprocal, once for all lanes, and broadcasts them
-        float mylo = 0.0f, myhi = 0.0f;
+        float mys, myz;
+        if constexpr (SYM) {
+            float mya = 0.0f;
 #pragma unroll
-        for (int u = 0; u < GPW; ++u) {
-            const float4 v = vv[u];
-            const float lo = warp_min(fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
-            const float hi = warp_max(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-            if (lane == u) {
-                mylo = lo;
-                myhi = hi;
+            for (int u = 0; u < GPW; ++u) {
+                const float4 v = vv[u];
+                const float a = warp_absmax(
+                    fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+                if (lane == u) mya = a;
             }
+            mys = __fdiv_rn(mya, 7.0f);
+            if (mys == 0.0f) mys = 1.0f;
+            myz = 8.0f;
+        } else {
+            float mylo = 0.0f, myhi = 0.0f;
+#pragma unroll
+            for (int u = 0; u < GPW; ++u) {
+                const float4 v = vv[u];
+                const float lo = warp_min(fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+                const float hi = warp_max(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                if (lane == u) {
+                    mylo = lo;
+                    myhi = hi;
+                }
+            }
+            // keep 0 exactly representable
+            mylo = fminf(mylo, 0.0f);
+            myhi = fmaxf(myhi, 0.0f);
+            mys = (myhi > mylo) ? __fdiv_rn(__fsub_rn(myhi, mylo), 15.0f) : 1.0f;
+            myz = fminf(fmaxf(roundf(__fdiv_rn(-mylo, mys)), 0.0f), 15.0f);
         }
-        // keep 0 exactly representable
-        mylo = fminf(mylo, 0.0f);
-        myhi = fmaxf(myhi, 0.0f);
-        const float mys = (myhi > mylo) ? __fdiv_rn(__fsub_rn(myhi, mylo), 15.0f) : 1.0f;
-        const float myz = fminf(fmaxf(roundf(__fdiv_rn(-mylo, mys)), 0.0f), 15.0f);
         const float myr = __frcp_rn(mys);
 #pragma unroll
         for (int u = 0; u < GPW; ++u) {
@@ -97,10 +155,12 @@ __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, i
             const float r = __shfl_sync(0xffffffffu, myr, u);
             const int zi = static_cast<int>(__shfl_sync(0xffffffffu, myz, u));
             // flat index gi*128 + 4*lane + i: even index in the low nibble
-            const uint32_t two = static_cast<uint32_t>(code_of(v.x, sc, r, zi)) |
-                                 (static_cast<uint32_t>(code_of(v.y, sc, r, zi)) << 4) |
-                                 (static_cast<uint32_t>(code_of(v.z, sc, r, zi)) << 8) |
-                                 (static_cast<uint32_t>(code_of(v.w, sc, r, zi)) << 12);
+            auto code = [&](float x) -> uint32_t {
+                if constexpr (SYM) return static_cast<uint32_t>(code_sym(x, sc, r));
+                else return static_cast<uint32_t>(code_of(x, sc, r, zi));
+            };
+            const uint32_t two =
+                code(v.x) | (code(v.y) << 4) | (code(v.z) << 8) | (code(v.w) << 12);
             reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = static_cast<uint16_t>(two);
             if (lane == u) {
                 scale[gi] = mys;
@@ -259,11 +319,14 @@ static int grid_for(int64_t work, int threads)
 }
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                            uint8_t *zero, cudaStream_t s)
+                            uint8_t *zero, bool symmetric, cudaStream_t s)
 {
     const int64_t ngroups = N * K / G;
-    k_quantize<<<grid_for((ngroups + GPW - 1) / GPW * 32, 256), 256, 0, s>>>(w, ngroups, packed,
-                                                                             scale, zero);
+    const int grid = grid_for((ngroups + GPW - 1) / GPW * 32, 256);
+    if (symmetric)
+        k_quantize<true><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero);
+    else
+        k_quantize<false><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero);
     return cudaGetLastError();
 }
 
