@@ -810,7 +810,8 @@ def gemm_case(args) -> int:
     assert q4.check() == q4.OK
     t = a.elapsed_time(b) / 1e3 / args.reps
     print(json.dumps({"gemm_case": f"{M}x{N}x{K}", "ms": round(t * 1e3, 3),
-                      "TFLOP/s": round(2.0 * M * N * K / t / 1e12, 1)}), flush=True)
+                      "TFLOP/s": round(2.0 * M * N * K / t / 1e12, 1),
+                      "GB/s": round(algo_bytes(M, N, K) / t / 1e9, 1)}), flush=True)
     return 0
 
 

@@ -27,13 +27,15 @@ def test_gemm_parity(M, N, K, xdt):
         compare(y, y_ref, absdot, where=f"gemm {M}x{N}x{K} y={ydt}")
 
 
-@pytest.mark.parametrize("M", [1, 17, 32])
+@pytest.mark.parametrize("M", [1, 9, 16, 17, 32, 48, 64, 100, 128, 129, 255])
 def test_gemm_small_m(M):
-    """q4_gemm accepts any M >= 1; a batch far below one 256-token tile."""
+    """q4_gemm accepts any M >= 1; the token tile (16, 32, 64, 128 or 256
+    rows) is the smallest that covers M, with a ragged last tile."""
     import weight_only_int4_group_gb300 as q4
     N, K = 384, 2048
     W = synth.normal_rows(M + 11, K, 0, N, 0.02)
-    x, xf = x_for(torch.bfloat16, M, K, seed=M + 3)
+    xdt = torch.float16 if M in (9, 100) else torch.bfloat16
+    x, xf = x_for(xdt, M, K, seed=M + 3)
     _, y_ref, absdot = oracle_product(W, xf)
     y = q4.gemm(x, q4.QWeight.from_float(dev_f32(W)), out_dtype=torch.bfloat16)
     torch.cuda.synchronize()

@@ -6,24 +6,36 @@
 // same pass (page "LLM Quantization Architecture in Depth", "Kernels and
 // memory layout"); the fp weights never reach HBM.
 //
-// One persistent CTA per SM, 14 warps with fixed roles:
-//   warp 0     producer: activation tiles by 2-D tensor TMA (128-byte
-//              swizzle) and packed weight tiles by 1-D bulk copies;
+// One persistent CTA per SM, 15 warps with fixed roles:
+//   warp 0     activation producer: tiles of X by 2-D tensor TMA (128-byte
+//              swizzle);
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma;
 //   warps 2-9  dequantize, one 16-row tile each: codes -> bf16 (or f16)
 //              w_hat = (q - zero) * scale, written in the K-major
 //              128-byte-swizzled layout the MMA reads;
 //   warps 10-13 epilogue: tcgen05.ld of the accumulators -> bf16/f16 ->
 //              coalesced stores (32 consecutive outputs of one token per
-//              warp instruction).
-// CTA tile: 128 weight rows x 256 tokens, K in stages of 64.  The MMA computes
-// the transposed product Y^T = W_hat * X^T: A = the dequantized weight tile
-// (128 rows), B = the 256 activation rows, one 128 x 256 x 16 MMA per 16 k,
-// so each weight tile is dequantized once per 256 tokens.  Accumulator:
-// 128 lanes x 256 f32 columns in tensor memory, double-buffered (512
-// columns) so the epilogue of one tile overlaps the MMAs of the next.  Every barrier wait is bounded; on expiry the CTA
-// raises the device error word, stops, drains its copies and MMAs, frees its
-// tensor memory and returns.
+//              warp instruction);
+//   warp 14    weight producer: packed tiles by 1-D bulk copies, in its own
+//              ring, so the weight stream runs as far ahead as its ring
+//              allows whatever the activation ring is doing.
+// CTA tile: 128 weight rows x BT tokens, K in stages of one group (128),
+// where BT is the smallest of 16, 32, 64, 128 and 256 that covers M (256 for
+// larger M): a few tokens get a narrow MMA and a short activation box
+// instead of a 256-row one that is mostly padding.  The MMA computes the
+// transposed product Y^T = W_hat * X^T: A = the dequantized weight tile (128
+// rows), B = the BT activation rows, one 128 x BT x 16 MMA per 16 k, so each
+// weight tile is dequantized once per BT tokens.  A stage holds one group's
+// activations and its dequantized weights under one "full" barrier (the
+// activation bytes plus the eight dequantizing warps) and one "empty"
+// barrier (the MMAs that read it): a barrier wait costs the waiting thread
+// a few hundred cycles even when the phase is already complete, so the MMA
+// thread waits once and commits once per eight MMAs.  Accumulator: 128
+// lanes x BT f32 columns in tensor memory, double-buffered (buffers 256
+// columns apart) so the epilogue of one tile overlaps the MMAs of the next.
+// Every barrier wait is bounded; on expiry the CTA raises the device error
+// word, stops, drains its copies and MMAs, frees its tensor memory and
+// returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,25 +47,37 @@ namespace q4 {
 namespace gm {
 
 constexpr int BM = 256, SUB = 128, BN = 128, BK = 64;
-constexpr int NA = 4;   // activation stages (latency of the L2 reads of X)
-constexpr int NBS = 4;  // dequantized-weight stages
-constexpr int NC = 2;   // packed-code stages (one group = two k stages)
+constexpr int NARROW_MAX = 64;             // token tiles up to this use the narrow plan
 constexpr int RT = BN / TILE_ROWS;         // 8 row tiles per weight tile
 constexpr int A_BOX = SUB * BK * 2;        // 16384: one 128 x 64 activation box
-constexpr int A_STAGE = 2 * A_BOX;         // 32768
-constexpr int B_STAGE = BN * BK * 2;       // 16384
-constexpr int C_STAGE = RT * TILE_BYTES;   // 8832
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NA * A_STAGE;
-constexpr int OFF_C = OFF_B + NBS * B_STAGE;
-constexpr int OFF_BAR = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;
-constexpr int SMEM_USED = OFF_BAR + 256;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
-constexpr int THREADS = 448;
+constexpr int B_HALF = BN * BK * 2;        // 16384: dequantized weights of 64 k
+constexpr int C_STAGE = RT * TILE_BYTES;   // 8832: packed tiles of one group
+constexpr int THREADS = 480;
 constexpr uint32_t TMEM_COLS = 512;
 
-static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0, "alignment");
-static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
+// Shared-memory plan of one CTA: NS stages of one group each (activations in
+// two 64-wide swizzled halves, then the dequantized weights in two halves),
+// NC packed-code stages.  The narrow plan (token tiles of at most 64 rows)
+// needs 8 KB activation halves and keeps 4 stages; the wide plan 32 KB
+// halves and 2 stages (the same 256 k of lookahead).
+template <bool NARROW>
+struct Plan {
+    static constexpr int NS = NARROW ? 4 : 2;
+    static constexpr int NC = 3;
+    static constexpr int A_HALF = NARROW ? NARROW_MAX * BK * 2 : 2 * A_BOX;
+    static constexpr int A_ST = 2 * A_HALF;
+    static constexpr int B_ST = 2 * B_HALF;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + NS * A_ST;
+    static constexpr int OFF_C = OFF_B + NS * B_ST;
+    static constexpr int OFF_BAR = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;
+    static constexpr int BAR_BYTES = (2 * (NS + NC) + 5) * 8 + 8;
+    static constexpr int SMEM_USED = OFF_BAR + 256;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+    static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0, "alignment");
+    static_assert(BAR_BYTES <= 256, "barrier area");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
+};
 
 // ----------------------------------------------------------------- PTX
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
@@ -98,10 +122,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
 }
 
 // Instruction descriptor, kind::f16: f32 accumulate, A/B bf16 (ab = 1) or
-// f16 (ab = 0), both K-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab)
+// f16 (ab = 0), both K-major, M = 128, N = n (a multiple of 16, 16..256).
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab, uint32_t n)
 {
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -155,27 +179,30 @@ struct Args {
     const uint8_t *qw;
     void *y;
     int M, N, K;
-    int mt, nt;  // tiles along M (256 rows) and N (128 rows)
+    int bt;      // tokens per tile: 16, 32, 64, 128 or 256
+    int mt, nt;  // tiles along M (bt rows) and N (128 rows)
     uint64_t wait_ns;
     unsigned int *err;
 };
 
 // F16: activations (and the dequantized weights) are f16, else bf16.
-// YF16: outputs are f16, else bf16.
-template <bool F16, bool YF16>
+// YF16: outputs are f16, else bf16.  NARROW: the shared-memory plan for
+// token tiles of at most 64 rows.
+template <bool F16, bool YF16, bool NARROW>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmx, const Args a)
 {
+    using P = Plan<NARROW>;
+    constexpr int NS = P::NS, NC = P::NC, A_HALF = P::A_HALF, A_ST = P::A_ST, B_ST = P::B_ST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sA = smem + OFF_A;
-    uint8_t *sB = smem + OFF_B;
-    uint8_t *sC = smem + OFF_C;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full_a = bar, *empty_a = bar + NA;
-    uint64_t *full_b = bar + 2 * NA, *empty_b = full_b + NBS;
-    uint64_t *full_c = empty_b + NBS, *empty_c = full_c + NC;
+    uint8_t *sA = smem + P::OFF_A;
+    uint8_t *sB = smem + P::OFF_B;
+    uint8_t *sC = smem + P::OFF_C;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
+    uint64_t *full = bar, *empty = bar + NS;
+    uint64_t *full_c = empty + NS, *empty_c = full_c + NC;
     uint64_t *acc_full = empty_c + NC, *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -183,18 +210,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
-    const int KS = a.K / BK;
     const int ntiles_rows = (a.N + TILE_ROWS - 1) / TILE_ROWS;
     const int T = a.mt * a.nt;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NA; ++i) {
-            mbar_init(&full_a[i], 1);
-            mbar_init(&empty_a[i], 1);
-        }
-        for (int i = 0; i < NBS; ++i) {
-            mbar_init(&full_b[i], 8);
-            mbar_init(&empty_b[i], 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1 + 8);  // activation producer + dequantizing warps
+            mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < NC; ++i) {
             mbar_init(&full_c[i], 1);
@@ -215,84 +237,99 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer
+        // ------------------------------------------------- activation producer
         if (lane == 0) {
-            int ia = 0, ic = 0;
+            int is = 0;
             bool ok = true;
+            // per 64-k half: one box of bt rows, or two of SUB rows when bt = 256
+            const int nbox = a.bt > SUB ? 2 : 1;
+            const uint32_t st_bytes = 2u * static_cast<uint32_t>(a.bt) * BK * 2;
             for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
-                const int m0 = (tile % a.mt) * BM, nb = tile / a.mt;
-                const int rt0 = nb * RT, nrt = min(RT, ntiles_rows - rt0);
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int sa = ia % NA;
-                    if (ia >= NA && !mbar_wait_bounded(&empty_a[sa], ((ia / NA) - 1) & 1, abort_flag,
+                const int m0 = (tile % a.mt) * a.bt;
+                for (int g = 0; g < NG; ++g) {
+                    const int s = is % NS;
+                    if (is >= NS && !mbar_wait_bounded(&empty[s], ((is / NS) - 1) & 1, abort_flag,
                                                        a.wait_ns, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_a[sa], A_STAGE);
-                    tma_load_2d(sA + sa * A_STAGE, &tmx, ks * BK, m0, &full_a[sa]);
-                    tma_load_2d(sA + sa * A_STAGE + A_BOX, &tmx, ks * BK, m0 + SUB, &full_a[sa]);
-                    ++ia;
-                    if ((ks & 1) == 0) {
-                        const int sc = ic % NC;
-                        if (ic >= NC && !mbar_wait_bounded(&empty_c[sc], ((ic / NC) - 1) & 1,
-                                                           abort_flag, a.wait_ns, a.err)) {
-                            ok = false;
-                            break;
-                        }
-                        const int g = ks >> 1;
-                        mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TILE_BYTES);
-                        for (int r = 0; r < nrt; ++r)
-                            bulk_g2s(sC + sc * C_STAGE + r * TILE_BYTES,
-                                     a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TILE_BYTES,
-                                     TILE_BYTES, &full_c[sc]);
-                        ++ic;
+                    mbar_arrive_expect_tx(&full[s], st_bytes);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint8_t *dst = sA + s * A_ST + h * A_HALF;
+                        tma_load_2d(dst, &tmx, g * G + h * BK, m0, &full[s]);
+                        if (nbox == 2) tma_load_2d(dst + A_BOX, &tmx, g * G + h * BK, m0 + SUB, &full[s]);
                     }
+                    ++is;
                 }
             }
             // every issued copy lands before the CTA may exit
-            for (int i = max(0, ia - NA); i < ia; ++i)
-                mbar_wait_bounded(&full_a[i % NA], (i / NA) & 1, abort_flag, a.wait_ns, a.err, false);
+            for (int i = max(0, is - NS); i < is; ++i)
+                mbar_wait_bounded(&full[i % NS], (i / NS) & 1, abort_flag, a.wait_ns, a.err, false);
+        }
+    } else if (warp == 14) {
+        // ----------------------------------------------------- weight producer
+        if (lane == 0) {
+            int ic = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
+                const int rt0 = (tile / a.mt) * RT, nrt = min(RT, ntiles_rows - rt0);
+                for (int g = 0; g < NG; ++g) {
+                    const int sc = ic % NC;
+                    if (ic >= NC && !mbar_wait_bounded(&empty_c[sc], ((ic / NC) - 1) & 1, abort_flag,
+                                                       a.wait_ns, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TILE_BYTES);
+                    for (int r = 0; r < nrt; ++r)
+                        bulk_g2s(sC + sc * C_STAGE + r * TILE_BYTES,
+                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TILE_BYTES,
+                                 TILE_BYTES, &full_c[sc]);
+                    ++ic;
+                }
+            }
             for (int i = max(0, ic - NC); i < ic; ++i)
                 mbar_wait_bounded(&full_c[i % NC], (i / NC) & 1, abort_flag, a.wait_ns, a.err, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(F16 ? 0u : 1u);
-            int ia = 0, ib = 0, tt = 0;
+            const uint32_t idesc = idesc_f16(F16 ? 0u : 1u, static_cast<uint32_t>(a.bt));
+            int is = 0, tt = 0;
             bool issued = false, ok = true;
             for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
                 const int buf = tt & 1;
                 if (tt >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((tt >> 1) - 1) & 1, abort_flag,
-                                                  a.wait_ns, a.err, true, true)) {
+                                                  a.wait_ns, a.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 256;
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int sa = ia % NA, sb = ib % NBS;
-                    if (!mbar_wait_bounded(&full_a[sa], (ia / NA) & 1, abort_flag, a.wait_ns, a.err, true, true) ||
-                        !mbar_wait_bounded(&full_b[sb], (ib / NBS) & 1, abort_flag, a.wait_ns, a.err, true, true)) {
+                for (int g = 0; g < NG; ++g) {
+                    const int s = is % NS;
+                    if (!mbar_wait_bounded(&full[s], (is / NS) & 1, abort_flag, a.wait_ns, a.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // A operand: the weight tile; B operand: the 256
-                    // activation rows (two TMA boxes, contiguous)
-                    const uint32_t xa = smem_u32(sA + sa * A_STAGE);
-                    const uint32_t wb = smem_u32(sB + sb * B_STAGE);
+                    // A operand: the weight tile; B operand: the bt activation
+                    // rows (one TMA box, or two contiguous ones); per 64-k half
+                    // four MMAs of k = 16
+                    const uint32_t xa = smem_u32(sA + s * A_ST);
+                    const uint32_t wb = smem_u32(sB + s * B_ST);
 #pragma unroll
-                    for (int k16 = 0; k16 < BK / 16; ++k16) {
-                        const uint32_t acc = (ks > 0 || k16 > 0) ? 1u : 0u;
-                        mma_f16(d, sw128_desc(wb + 32 * k16), sw128_desc(xa + 32 * k16), idesc, acc);
-                    }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int k16 = 0; k16 < BK / 16; ++k16) {
+                            const uint32_t acc = (g > 0 || h > 0 || k16 > 0) ? 1u : 0u;
+                            mma_f16(d, sw128_desc(wb + h * B_HALF + 32 * k16),
+                                    sw128_desc(xa + h * A_HALF + 32 * k16), idesc, acc);
+                        }
                     issued = true;
-                    mma_commit(&empty_a[sa]);
-                    mma_commit(&empty_b[sb]);
-                    ++ia;
-                    ++ib;
+                    mma_commit(&empty[s]);
+                    ++is;
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[buf]);
@@ -306,35 +343,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < 10) {
         // ------------------------------------------------------ dequantize
         const int d = warp - 2, gq = lane >> 2, t = lane & 3;
-        int ib = 0, ic = 0;
+        int is = 0, ic = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
             const int nb = tile / a.mt;
             const int nrt = min(RT, ntiles_rows - nb * RT);
-            for (int ks = 0; ks < KS; ++ks) {
-                const int h = ks & 1, sc = ic % NC, sb = ib % NBS;
-                if (h == 0)
-                    ok = mbar_wait_bounded(&full_c[sc], (ic / NC) & 1, abort_flag, a.wait_ns, a.err);
-                if (ok && ib >= NBS)
-                    ok = mbar_wait_bounded(&empty_b[sb], ((ib / NBS) - 1) & 1, abort_flag, a.wait_ns,
+            for (int g = 0; g < NG; ++g) {
+                const int s = is % NS, sc = ic % NC;
+                ok = mbar_wait_bounded(&full_c[sc], (ic / NC) & 1, abort_flag, a.wait_ns, a.err);
+                if (ok && is >= NS)
+                    ok = mbar_wait_bounded(&empty[s], ((is / NS) - 1) & 1, abort_flag, a.wait_ns,
                                            a.err);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
-                uint8_t *bst = sB + sb * B_STAGE;
+                if (d < nrt) {
+                    const uint8_t *ct = sC + sc * C_STAGE + d * TILE_BYTES;
+                    const float2 sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
+                    const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
+                    const float nz0 = -(128.0f + static_cast<float>(zp & 0xFFu));
+                    const float nz8 = -(128.0f + static_cast<float>(zp >> 8));
 #pragma unroll
-                for (int rr = 0; rr < 1; ++rr) {
-                    const int r = d + rr;
-                    if (r < nrt) {
-                        const uint8_t *ct = sC + sc * C_STAGE + r * TILE_BYTES;
+                    for (int h = 0; h < 2; ++h) {
                         const uint4 cw = *reinterpret_cast<const uint4 *>(ct + h * 512 + 16 * lane);
-                        const float2 sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
-                        const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
-                        const float nz0 = -(128.0f + static_cast<float>(zp & 0xFFu));
-                        const float nz8 = -(128.0f + static_cast<float>(zp >> 8));
                         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-                        uint8_t *row0 = bst + (16 * r + gq) * 128 + 4 * t;
+                        uint8_t *row0 = sB + s * B_ST + h * B_HALF + (16 * d + gq) * 128 + 4 * t;
                         uint8_t *row8 = row0 + 8 * 128;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -353,15 +387,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_b[sb]);
-                ++ib;
-                if (h == 1) {
-                    if (lane == 0) mbar_arrive(&empty_c[sc]);
-                    ++ic;
+                if (lane == 0) {
+                    mbar_arrive(&full[s]);
+                    mbar_arrive(&empty_c[sc]);
                 }
+                ++is;
+                ++ic;
             }
         }
-    } else {
+    } else if (warp < 14) {
         // ------------------------------------------------------ epilogue
         // Warp p reads tensor-memory lanes 32p..32p+31 (weight rows n0 + 32p
         // + lane); each 32-column load gives a lane 32 consecutive tokens, and
@@ -370,7 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int tt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
-            const int m0 = (tile % a.mt) * BM, n0 = (tile / a.mt) * BN;
+            const int m0 = (tile % a.mt) * a.bt, n0 = (tile / a.mt) * BN;
             const int buf = tt & 1;
             ok = mbar_wait_bounded(&acc_full[buf], (tt >> 1) & 1, abort_flag, a.wait_ns, a.err);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -381,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int n = n0 + 32 * p + lane;
             uint16_t *ycol = reinterpret_cast<uint16_t *>(a.y) + n;
 #pragma unroll 1
-            for (int c = 0; c < BM / 32; ++c) {
+            for (int c = 0; c < (a.bt + 31) / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * p) << 16) + buf * 256 + 32 * c, v);
                 const int mb = m0 + 32 * c;
@@ -452,33 +486,42 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
     *cerr = cudaSuccess;
     const bool f16 = (xt == Q4_F16);
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    int bt = 16;
+    while (bt < BM && bt < M) bt *= 2;
+    const bool narrow = bt <= NARROW_MAX;
     CUtensorMap tmx;
-    if (!make_map(&tmx, x, dt, K, M, K * 2, BK, SUB)) return Q4_ERR_UNSUPPORTED;
+    if (!make_map(&tmx, x, dt, K, M, K * 2, BK, bt < SUB ? bt : SUB)) return Q4_ERR_UNSUPPORTED;
     Args a{};
     a.qw = static_cast<const uint8_t *>(qw);
     a.y = y;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.mt = static_cast<int>((M + BM - 1) / BM);
+    a.bt = bt;
+    a.mt = static_cast<int>((M + bt - 1) / bt);
     a.nt = static_cast<int>((N + BN - 1) / BN);
     a.wait_ns = 2000000000ull;
     a.err = err;
     const int tiles = a.mt * a.nt;
     const int grid = tiles < sm_count ? tiles : sm_count;
     const bool yf16 = (yt == Q4_F16);
-    auto kern = f16 ? (yf16 ? k_gemm<true, true> : k_gemm<true, false>)
-                    : (yf16 ? k_gemm<false, true> : k_gemm<false, false>);
-    const int variant = (f16 ? 2 : 0) + (yf16 ? 1 : 0);
-    static std::atomic<bool> configured[4][64];  // concurrent first calls may both set it
+    using KernFn = void (*)(CUtensorMap, Args);
+    static const KernFn kerns[8] = {
+        k_gemm<false, false, false>, k_gemm<false, true, false>, k_gemm<true, false, false>,
+        k_gemm<true, true, false>,   k_gemm<false, false, true>, k_gemm<false, true, true>,
+        k_gemm<true, false, true>,   k_gemm<true, true, true>};
+    const int variant = (narrow ? 4 : 0) + (f16 ? 2 : 0) + (yf16 ? 1 : 0);
+    const KernFn kern = kerns[variant];
+    const int smem = narrow ? Plan<true>::SMEM_ALLOC : Plan<false>::SMEM_ALLOC;
+    static std::atomic<bool> configured[8][64];  // concurrent first calls may both set it
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[variant][dev].load(std::memory_order_relaxed)) {
-        *cerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        *cerr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
         if (dev >= 0 && dev < 64) configured[variant][dev].store(true, std::memory_order_relaxed);
     }
-    kern<<<grid, THREADS, SMEM_ALLOC, s>>>(tmx, a);
+    kern<<<grid, THREADS, smem, s>>>(tmx, a);
     *cerr = cudaGetLastError();
     return *cerr == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
