@@ -305,6 +305,22 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(torch, dist, ws: int, v: float, device) -> float:
+    """The largest of every rank's `v` (the slowest replica's time): one
+    all-reduce; no collective at all for a single process."""
+    if ws == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(ws: int, bytes_per_replica: int, t_slowest: float) -> float:
+    """Aggregate GB/s of `ws` independent replicas, each moving
+    `bytes_per_replica` per step, timed by the slowest one."""
+    return ws * bytes_per_replica / t_slowest / 1e9
+
+
 def reference_arm(args, ws, rank):
     """The oracle, as it stands, on the host cores: each step is one pass of
     the page's factored dot over layer 0 of the workload (all four
@@ -398,15 +414,11 @@ def main():
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
-    if ws > 1:
-        t = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
+    t_step = max_over_ranks(torch, dist, ws, ev0.elapsed_time(ev1) / 1e3 / args.steps, "cuda")
     assert q4.check() == q4.OK, "device error during the timed region"
     clocks = clk.summary()
 
-    value = ws * work.bytes_per_step / t_step / 1e9
+    value = whole_job_gbs(ws, work.bytes_per_step, t_step)
     achieved = work.bytes_per_step / t_step / 1e9
     traffic = profile_traffic("gemv_decode70b_M1.md", GEMV_SOURCES) if args.M == 1 else None
 
@@ -430,12 +442,8 @@ def main():
             hy.copy_(work.y, non_blocking=True)
         b.record(st)
         b.synchronize()
-        t_e2e = a.elapsed_time(b) / 1e3 / reps
-        if ws > 1:
-            t = torch.tensor([t_e2e], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": round(ws * work.bytes_per_step / t_e2e / 1e9, 2), "unit": "GB/s",
+        t_e2e = max_over_ranks(torch, dist, ws, a.elapsed_time(b) / 1e3 / reps, "cuda")
+        e2e = {"value": round(whole_job_gbs(ws, work.bytes_per_step, t_e2e), 2), "unit": "GB/s",
                "h2d_bytes_per_step": work.x_elems * 2, "d2h_bytes_per_step": work.y_elems * 2,
                "ms_per_step": round(t_e2e * 1e3, 4), "api": "q4_gemv eager, 320 calls"}
 

@@ -188,7 +188,9 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
  * f16 activations) and multiplied on the tcgen05 tensor cores with f32
  * accumulators in tensor memory.  x: [M][K] BF16 or F16; y: [M][N] BF16 or
  * F16 (f32 is UNSUPPORTED here).  Requires M >= 1, N % 16 == 0; x, qw and y
- * 16-byte aligned.  Each w_hat is rounded once to the activation type, so the
+ * 16-byte aligned.  Any M: each CTA tile covers 128 weight rows and the
+ * smallest of 16, 32, 64, 128 or 256 tokens that covers M (256 beyond), so
+ * a batch of a few dozen tokens costs a narrow MMA, not a 256-token one.  Each w_hat is rounded once to the activation type, so the
  * product differs from the exact dequantized product by at most one rounding
  * of each w_hat (2^-9 relative for bf16) -- statistically far below
  * 1e-3 * sum|w_hat x| for non-adversarial data.

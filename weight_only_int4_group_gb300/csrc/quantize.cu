@@ -17,26 +17,20 @@
 
 namespace q4 {
 
-// Warp-wide minimum / maximum of one finite f32 per lane, exact for every
-// finite value (subnormals included): the reduction runs on integer keys whose
-// signed order is the float order (positive floats keep their bits, negative
-// ones flip their magnitude bits; the map is its own inverse).
-__device__ __forceinline__ int order_key(float v)
-{
-    const int b = __float_as_int(v);
-    return b ^ ((b >> 31) & 0x7fffffff);
-}
+// Warp-wide minimum / maximum of one f32 per lane (exact selections;
+// subnormal values come through unchanged -- groups made of subnormals
+// quantize bit-identically to the oracle).
 __device__ __forceinline__ float warp_min(float v)
 {
-    int r;
-    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(order_key(v)));
-    return __int_as_float(r ^ ((r >> 31) & 0x7fffffff));
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ float warp_max(float v)
 {
-    int r;
-    asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(order_key(v)));
-    return __int_as_float(r ^ ((r >> 31) & 0x7fffffff));
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 // Warp-wide maximum of one |w| per lane: for non-negative floats the bit
 // patterns are ordered like the values.
