@@ -65,6 +65,14 @@ class Oracle:
         lib.oq4_dot_factored.restype = None
         lib.oq4_xsum.argtypes = [_P, _I, _I, _P]
         lib.oq4_xsum.restype = None
+        lib.oq4_f16_bits.argtypes = [ctypes.c_float]
+        lib.oq4_f16_bits.restype = ctypes.c_uint16
+        lib.oq4_f16_value.argtypes = [ctypes.c_uint16]
+        lib.oq4_f16_value.restype = ctypes.c_float
+        lib.oq4_compact_meta.argtypes = [_P, _P, _I, _I, _P, _P]
+        lib.oq4_compact_meta.restype = None
+        lib.oq4_expand_meta.argtypes = [_P, _P, _I, _I, _P, _P]
+        lib.oq4_expand_meta.restype = None
         lib.oq4_mutant.restype = ctypes.c_int
         self.lib = lib
         self.path = path
@@ -88,6 +96,37 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle quantize rejected shape {N}x{K} with G={group}")
         return packed, scale, zero
+
+    # -- compact metadata (binary16 scales, 4-bit zeros) ---------------------
+    def f16_bits(self, v: np.ndarray) -> np.ndarray:
+        v = np.ascontiguousarray(v, np.float32).reshape(-1)
+        return np.array([self.lib.oq4_f16_bits(float(x)) for x in v], np.uint16)
+
+    def f16_values(self, h: np.ndarray) -> np.ndarray:
+        h = np.ascontiguousarray(h, np.uint16).reshape(-1)
+        return np.array([self.lib.oq4_f16_value(int(x)) for x in h], np.float32)
+
+    def compact_meta(self, scale, zero):
+        """scale f32 [N][NG], zero u8 [N][NG] -> (scale16 u16 [N][NG], zero4 u8 [N][ceil(NG/2)])."""
+        scale = np.ascontiguousarray(scale, np.float32)
+        zero = np.ascontiguousarray(zero, np.uint8)
+        N, NG = scale.shape
+        s16 = np.empty((N, NG), np.uint16)
+        z4 = np.empty((N, (NG + 1) // 2), np.uint8)
+        self.lib.oq4_compact_meta(scale.ctypes.data, zero.ctypes.data, N, NG, s16.ctypes.data,
+                                  z4.ctypes.data)
+        return s16, z4
+
+    def expand_meta(self, scale16, zero4, NG: int):
+        """Inverse containers: (scale f32 [N][NG] widened from binary16, zero u8 [N][NG])."""
+        scale16 = np.ascontiguousarray(scale16, np.uint16)
+        zero4 = np.ascontiguousarray(zero4, np.uint8)
+        N = scale16.shape[0]
+        scale = np.empty((N, NG), np.float32)
+        zero = np.empty((N, NG), np.uint8)
+        self.lib.oq4_expand_meta(scale16.ctypes.data, zero4.ctypes.data, N, NG, scale.ctypes.data,
+                                 zero.ctypes.data)
+        return scale, zero
 
     def dequant(self, packed, scale, zero, N: int, K: int, group: int = G) -> np.ndarray:
         packed = np.ascontiguousarray(packed, np.uint8)

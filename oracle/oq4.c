@@ -277,3 +277,87 @@ void oq4_xsum(const float *x, int64_t M, int64_t K, double *xsum)
             xsum[m * NG + g] = s;
         }
 }
+
+/* ---------------------------------------------------------------------------
+ * Compact metadata (page "Weight quantization", section "Code": the bits per
+ * weight it prints count each scale as 16 bits and each zero as 4 bits;
+ * section "Complexity and constants": int4 g128 with an fp16 scale and a
+ * 4-bit zero; "Implementation notes": keep scales in fp16/bf16).  The codes
+ * and zeros are the canonical ones; the scale is stored rounded once to IEEE
+ * binary16 (round to nearest, ties to even), and the zeros two per byte. */
+
+/* f32 -> binary16 bits, round to nearest even; overflow gives infinity. */
+uint16_t oq4_f16_bits(float v)
+{
+    uint32_t x;
+    memcpy(&x, &v, sizeof x);
+    const uint32_t sign = (x >> 16) & 0x8000u;
+    const uint32_t ex = (x >> 23) & 0xFFu;
+    uint32_t man = x & 0x7FFFFFu;
+    if (ex == 0xFFu) return (uint16_t)(sign | 0x7C00u | (man ? 0x200u : 0u));
+    const int e = (int)ex - 127 + 15;  /* binary16 biased exponent */
+    if (e >= 31) return (uint16_t)(sign | 0x7C00u);
+    if (e <= 0) {
+        /* binary16 subnormal (or zero): units of 2^-24 */
+        if (ex == 0) return (uint16_t)sign;  /* f32 subnormals are below 2^-126 */
+        man |= 0x800000u;
+        const int shift = 14 - e;
+        if (shift > 24) return (uint16_t)sign;
+        uint32_t q = man >> shift;
+        const uint32_t rem = man & ((1u << shift) - 1u), half = 1u << (shift - 1);
+#if OQ4_MUTANT != 15
+        if (rem > half || (rem == half && (q & 1u))) ++q;
+#endif
+        return (uint16_t)(sign | q);
+    }
+    uint32_t q = ((uint32_t)e << 10) | (man >> 13);
+    const uint32_t rem = man & 0x1FFFu;
+#if OQ4_MUTANT != 15
+    if (rem > 0x1000u || (rem == 0x1000u && (q & 1u))) ++q;  /* a carry may reach infinity */
+#endif
+    return (uint16_t)(sign | q);
+}
+
+/* binary16 bits -> f32 (exact). */
+float oq4_f16_value(uint16_t h)
+{
+    const int sign = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return (float)(sign ? -v : v);
+}
+
+void oq4_compact_meta(const float *scale, const uint8_t *zero, int64_t N, int64_t NG,
+                      uint16_t *scale16, uint8_t *zero4)
+{
+    const int64_t ZB = (NG + 1) / 2;
+    memset(zero4, 0, (size_t)(N * ZB));
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < NG; ++g) {
+            scale16[n * NG + g] = oq4_f16_bits(scale[n * NG + g]);
+#if OQ4_MUTANT == 16
+            const int hi = !(g & 1);
+#else
+            const int hi = (int)(g & 1);
+#endif
+            zero4[n * ZB + g / 2] |= (uint8_t)((zero[n * NG + g] & 0x0F) << (4 * hi));
+        }
+}
+
+void oq4_expand_meta(const uint16_t *scale16, const uint8_t *zero4, int64_t N, int64_t NG,
+                     float *scale, uint8_t *zero)
+{
+    const int64_t ZB = (NG + 1) / 2;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < NG; ++g) {
+            scale[n * NG + g] = oq4_f16_value(scale16[n * NG + g]);
+            const uint8_t b = zero4[n * ZB + g / 2];
+            zero[n * NG + g] = (g & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 0x0F);
+        }
+}
+

@@ -81,6 +81,21 @@ void oq4_dot_factored(const float *x, int64_t M,
 /* Activation group sums: xsum[m][g] = sum_{k in group g} x[m][k] (double). */
 void oq4_xsum(const float *x, int64_t M, int64_t K, double *xsum);
 
+/* Compact metadata (page "Weight quantization": the bits-per-weight formula
+ * of section "Code" counts 16-bit scales and 4-bit zeros; "Complexity and
+ * constants": fp16 scale + 4-bit zero; "Implementation notes": scales in
+ * fp16/bf16).  Same codes and zeros as the canonical form; each scale
+ * stored as binary16, rounded once to nearest even; zeros two per byte
+ * (low nibble = even group).  scale16 [N][NG], zero4 [N][ceil(NG/2)].  The
+ * products of a compact weight are those of the canonical containers that
+ * oq4_expand_meta returns (the binary16 scale widened exactly). */
+uint16_t oq4_f16_bits(float v);
+float oq4_f16_value(uint16_t h);
+void oq4_compact_meta(const float *scale, const uint8_t *zero, int64_t N, int64_t NG,
+                      uint16_t *scale16, uint8_t *zero4);
+void oq4_expand_meta(const uint16_t *scale16, const uint8_t *zero4, int64_t N, int64_t NG,
+                     float *scale, uint8_t *zero);
+
 /* Mutation id this build was compiled with (0 = the real oracle). */
 int oq4_mutant(void);
 

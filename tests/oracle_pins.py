@@ -350,6 +350,87 @@ def pin_sym_half_step_and_nearest(o):
     assert (chosen <= dist.min(axis=2) + 2.0 ** -20 * s + 2.0 ** -22 * np.abs(Wd)).all()
 
 
+
+# ------------------------------------------------- compact metadata (fp16, 4-bit)
+# Page cited: "Weight quantization", section "Code" (bits per weight with
+# 16-bit scales and 4-bit zeros), "Complexity and constants" (fp16 scale +
+# 4-bit zero), "Implementation notes" (scales in fp16/bf16).
+
+def pin_f16_rounding_library(o):
+    """binary16 rounding against numpy's float16 conversion (IEEE round to
+    nearest even): random finite f32 bit patterns over the whole range, every
+    midpoint between neighbouring binary16 values (ties), the overflow edge;
+    and the exact widening of all 63488 finite binary16 patterns."""
+    rng = np.random.default_rng(31)
+    bits = rng.integers(0, 0xFF000000, 200_000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]
+    # keep most samples near binary16's range, where rounding is not trivial
+    near = (rng.integers(0x30000000, 0x48000000, 200_000, dtype=np.uint64).astype(np.uint32)
+            | (rng.integers(0, 2, 200_000, dtype=np.uint64).astype(np.uint32) << 31))
+    h = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)  # finite, non-negative
+    lo = h[:-1].view(np.float16).astype(np.float64)
+    hi = h[1:].view(np.float16).astype(np.float64)
+    mids = ((lo + hi) / 2).astype(np.float32)                     # exact in f32
+    mids = mids[mids.astype(np.float64) == (lo + hi) / 2]
+    edge = np.array([65504.0, 65519.996, 65520.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                     6.1035156e-05, 6.0975552e-05, 0.0, -0.0], np.float32)
+    v = np.concatenate([bits.view(np.float32), near.view(np.float32), mids, -mids, edge])
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(o.f16_bits(v), ref)
+    allh = np.concatenate([h, h | np.uint16(0x8000)])
+    assert np.array_equal(o.f16_values(allh).view(np.uint32),
+                          allh.view(np.float16).astype(np.float32).view(np.uint32))
+
+
+def pin_compact_meta_layout(o):
+    """Compacting keeps every zero (two per byte, even group in the low
+    nibble, an odd count padded with a zero nibble) and stores each scale as
+    its nearest-even binary16 (numpy's conversion); expanding widens it back
+    exactly."""
+    rng = np.random.default_rng(37)
+    for NG in (1, 2, 7, 64):
+        scale = rng.uniform(1e-4, 0.05, (5, NG)).astype(np.float32)
+        zero = rng.integers(0, 16, (5, NG)).astype(np.uint8)
+        s16, z4 = o.compact_meta(scale, zero)
+        assert np.array_equal(s16, scale.astype(np.float16).view(np.uint16))
+        zpad = np.concatenate([zero, np.zeros((5, NG % 2), np.uint8)], axis=1)
+        assert np.array_equal(z4, (zpad[:, 0::2] | (zpad[:, 1::2] << 4)).astype(np.uint8))
+        s2, z2 = o.expand_meta(s16, z4, NG)
+        assert np.array_equal(z2, zero)
+        assert np.array_equal(s2, scale.astype(np.float16).astype(np.float32))
+
+
+def pin_compact_bits_per_weight(o):
+    """The page's program counts 16-bit scales and 4-bit zeros: on its n =
+    4096 weights the compact arrays come to exactly its 4.15625 bits/weight."""
+    gold = read_golden("page_program.txt")
+    w, _ = synth.page_program(gold["n"])
+    packed, scale, zero = o.quantize(w)
+    s16, z4 = o.compact_meta(scale, zero)
+    bits = (packed.size * 8 + s16.size * 16 + z4.size * 8) / gold["n"]
+    assert bits == gold["bits_per_weight"]
+
+
+def pin_compact_error_bound(o):
+    """With the scale stored as binary16 (relative error at most 2^-11 in its
+    normal range) the reconstruction stays within half a step plus the
+    scale's rounding times the largest |q - zero| (15)."""
+    rng = np.random.default_rng(41)
+    W = rng.normal(0, 0.02, (32, 1024)).astype(np.float32)
+    W[0:4, ::37] *= np.float32(20.0)
+    N, K = W.shape
+    packed, scale, zero = o.quantize(W)
+    s16, z4 = o.compact_meta(scale, zero)
+    sc, zc = o.expand_meta(s16, z4, K // 128)
+    wh = o.dequant(packed, sc, zc, N, K)
+    s = np.repeat(scale.astype(np.float64), 128, axis=1)
+    ds = np.repeat(np.abs(sc.astype(np.float64) - scale.astype(np.float64)), 128, axis=1)
+    assert (np.abs(scale - sc) <= 2.0 ** -11 * scale).all()
+    err = np.abs(W.astype(np.float64) - wh)
+    assert (err <= 0.5 * s * (1 + 2 ** -16) + 15 * ds + 16 * np.abs(W) * 2.0 ** -24).all()
+
+
 ALL_PINS = [
     pin_page_program,
     pin_closed_form_integer_group,
@@ -367,4 +448,8 @@ ALL_PINS = [
     pin_sym_ties_to_even,
     pin_sym_special_groups,
     pin_sym_half_step_and_nearest,
+    pin_f16_rounding_library,
+    pin_compact_meta_layout,
+    pin_compact_bits_per_weight,
+    pin_compact_error_bound,
 ]

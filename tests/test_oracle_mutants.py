@@ -5,13 +5,14 @@ nibble for the even index, 4 no widening of the range to 0, 5 scale divided by
 16, 6 rounding after adding the zero, 7 zero from +lo, 8 factored dot without
 the zero term, 9 dequant with q + zero, 10 transposed weight operand, 11 wrong
 group index; symmetric scheme: 12 ties away from zero, 13 scale max|w|/8,
-14 codes stored as q + 7."""
+14 codes stored as q + 7; compact metadata: 15 binary16 by truncation, 16
+zero nibbles swapped."""
 import pytest
 
 import oracle
 from oracle_pins import ALL_PINS
 
-MUTANTS = list(range(1, 15))
+MUTANTS = list(range(1, 17))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
