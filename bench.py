@@ -580,6 +580,42 @@ def extra_rows(q4, torch, work, pk) -> dict:
         sweep[name] = res
     rows["mlp_sweep"] = sweep
 
+    # compact tiles (binary16 scales, 4-bit zeros) on 28672x8192: as many
+    # distinct copies as the sweep above used (far beyond L2, the same graph
+    # length); bytes counted as the compact tiles actually read, and the time
+    # per call set against the same M above
+    import synth
+    N, K, C = 28672, 8192, L
+    wf = torch.empty((N, K), dtype=torch.float32, device=dev)
+    synth.dev_normal_f32(wf.data_ptr(), N * K, 777, 0, SIGMA)
+    packed, scale, zero = q4.quantize(wf)
+    del wf
+    cqws = [q4.QWeight(q4.repack_compact(packed, scale, zero, N, K), N, K, compact=True)
+            for _ in range(C)]
+    del packed, scale, zero
+    cres = {}
+    for M in (1, 8, 16):
+        x = torch.empty(M * K, dtype=torch.int16, device=dev)
+        synth.dev_normal_bf16(x.data_ptr(), M * K, 4242 + M, 0, 1.0)
+        x = x.view(torch.bfloat16).view(M, K)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsp = torch.zeros(max(q4.gemv_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
+
+        def runc():
+            for c in range(C):
+                q4.gemv(x, cqws[c], out=y, ws=wsp)
+        g = graph_of(torch, runc)
+        t = time_graph(torch, g, reps=10) / C
+        b = q4.weight_bytes_compact(N, K) + M * K * 2 + M * N * 2
+        std = sweep["up 28672x8192"][f"M={M}"]["us_per_call"]
+        cres[f"M={M}"] = {"us_per_call": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                          "frac": round(b / t / 1e9 / pk["hbm_gbs"], 4),
+                          "speedup_vs_1104B_tiles": round(std / (t * 1e6), 4)}
+        del g
+    rows["compact_28672x8192"] = cres
+    del cqws
+    torch.cuda.empty_cache()
+
     # the decode step at M = 8 on the same weights (80 layers, one graph)
     M = 8
     import synth

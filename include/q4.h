@@ -67,6 +67,7 @@ typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
 #define Q4_GROUP 128
 #define Q4_TILE_ROWS 16
 #define Q4_TILE_BYTES 1104 /* 16 rows x 128 k: 1024 B codes + 64 B scales + 16 B zeros */
+#define Q4_CMP_TILE_BYTES 1072 /* compact: 1024 B codes + 32 B binary16 scales + 8 B zeros + 8 B pad */
 #define Q4_GEMV_MAX_M 16
 
 /*
@@ -120,6 +121,39 @@ q4_status q4_repack(const uint8_t *packed, const float *scale, const uint8_t *ze
 /* Tiled kernel layout -> canonical layout (exact inverse of q4_repack). */
 q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
                     uint8_t *zero, q4_stream_t stream);
+
+/*
+ * Compact metadata (page "Weight quantization": its printed bits per weight
+ * count 16-bit scales and 4-bit zeros, "Complexity and constants" names the
+ * fp16 scale + 4-bit zero format, "Implementation notes" keep scales in
+ * fp16/bf16).  Same codes and zeros as the canonical arrays; each scale is
+ * stored as IEEE binary16 rounded to nearest even (scales must lie in
+ * binary16's normal range, 6.1e-5 .. 65504, to keep their precision), so
+ * w_hat = (q - zero) * fp16(scale).  Tile (rt, g) at byte (rt*(K/128) + g) *
+ * 1072: bytes [0, 1024) codes exactly as in the tiled layout above; [1024,
+ * 1056) binary16 scale pairs (s[i], s[i+8]) for i = 0..7; [1056, 1064) one
+ * byte per pair, z[i] | z[i+8] << 4; [1064, 1072) zero padding (every tile
+ * stays 16-byte aligned).  4.1875 bits per weight in memory.
+ *
+ * q4_weight_bytes_compact: ceil(N/16) * (K/128) * 1072, 0 for invalid sizes.
+ * q4_repack_compact: canonical -> compact tiles; arguments, alignment and
+ *   errors as q4_repack.
+ * q4_unpack_compact: compact tiles -> codes [N][K/2], binary16 scale bits
+ *   scale16 [N][K/128], zeros [N][K/128] (one byte per group).
+ * q4_gemv_compact: q4_gemv on compact tiles (tensor-core path; same
+ *   arguments, workspace and errors; q4_gemv_workspace_bytes covers it).
+ * The layout of qw is not recorded in the buffer: compact tiles go to
+ * q4_gemv_compact only (q4_gemv, q4_gemv_path and q4_gemm read 1104-byte
+ * tiles and would read past the end of a compact buffer).
+ */
+size_t q4_weight_bytes_compact(int64_t N, int64_t K);
+q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                            int64_t N, int64_t K, void *qw, q4_stream_t stream);
+q4_status q4_unpack_compact(const void *qw, int64_t N, int64_t K, uint8_t *packed,
+                            uint16_t *scale16, uint8_t *zero, q4_stream_t stream);
+q4_status q4_gemv_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                          const void *qw, void *y, q4_dtype yt, void *workspace,
+                          size_t workspace_bytes, q4_stream_t stream);
 
 /*
  * Activation group sums, xsum[m][g] = sum_{k in group g} x[m][k] accumulated

@@ -72,6 +72,17 @@ def test_host_side_argument_errors(lib):
     assert lib.q4_quantize(fake, 0, 128, fake, fake, fake, None) == 1
     # misaligned input
     assert lib.q4_quantize(fake + 4, 4, 128, fake, fake, fake, None) == 3
+    # compact tiles: the same checks as the canonical layout
+    lib.q4_repack_compact.argtypes = [P, P, P, I, I, P, P]
+    lib.q4_gemv_compact.argtypes = [P, S, I, I, I, P, P, S, P, ctypes.c_size_t, P]
+    lib.q4_weight_bytes_compact.restype = ctypes.c_size_t
+    lib.q4_weight_bytes_compact.argtypes = [I, I]
+    assert lib.q4_weight_bytes_compact(17, 256) == 2 * 2 * 1072
+    assert lib.q4_weight_bytes_compact(16, 100) == 0
+    assert lib.q4_repack_compact(fake, fake, fake, 4, 128, fake + 8, None) == 3
+    assert lib.q4_repack_compact(fake, fake, fake, 4, 100, fake, None) == 1
+    assert lib.q4_gemv_compact(fake, 1, 17, 64, 128, fake, fake, 0, None, 0, None) == 2
+    assert lib.q4_gemv_compact(fake + 2, 1, 1, 64, 128, fake, fake, 0, None, 0, None) == 3
     # the symmetric quantizer shares the checks
     lib.q4_quantize_sym.argtypes = [P, I, I, P, P, P, P]
     assert lib.q4_quantize_sym(None, 4, 128, fake, fake, fake, None) == 1

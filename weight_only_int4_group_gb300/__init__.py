@@ -6,7 +6,9 @@ this package fails loudly when libq4.so has not been built; there is no
 fallback of any kind.
 
 Names follow include/q4.h: quantize, quantize_sym, repack, unpack, xsum,
-gemv, gemm, check, weight_bytes, gemv_workspace_bytes.
+gemv, gemm, check, weight_bytes, gemv_workspace_bytes, and the compact
+layout's weight_bytes_compact, repack_compact, unpack_compact (gemv on a
+compact QWeight calls q4_gemv_compact).
 """
 from __future__ import annotations
 
@@ -21,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libq4.so")
 GROUP = 128
 TILE_ROWS = 16
 TILE_BYTES = 1104
+CMP_TILE_BYTES = 1072
 GEMV_MAX_M = 16
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
@@ -51,6 +54,11 @@ def _load():
     lib.q4_weight_bytes.restype = Z
     lib.q4_repack.argtypes = [P, P, P, I, I, P, P]
     lib.q4_unpack.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_weight_bytes_compact.argtypes = [I, I]
+    lib.q4_weight_bytes_compact.restype = Z
+    lib.q4_repack_compact.argtypes = [P, P, P, I, I, P, P]
+    lib.q4_unpack_compact.argtypes = [P, I, I, P, P, P, P]
+    lib.q4_gemv_compact.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
     lib.q4_xsum.argtypes = [P, S, I, I, P, P]
     lib.q4_gemv_workspace_bytes.argtypes = [I, I, I]
     lib.q4_gemv_workspace_bytes.restype = Z
@@ -62,7 +70,8 @@ def _load():
     lib.q4_status_str.argtypes = [S]
     lib.q4_status_str.restype = ctypes.c_char_p
     lib.q4_last_cuda_error.restype = ctypes.c_char_p
-    for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_xsum", "q4_gemv", "q4_gemv_path",
+    for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_repack_compact",
+              "q4_unpack_compact", "q4_gemv_compact", "q4_xsum", "q4_gemv", "q4_gemv_path",
               "q4_gemv_timeout_selftest", "q4_gemm", "q4_check"):
         getattr(lib, f).restype = S
     return lib
@@ -97,6 +106,10 @@ def _cuda(t: torch.Tensor, name: str):
 # ------------------------------------------------------------------ API
 def weight_bytes(N: int, K: int) -> int:
     return int(_lib.q4_weight_bytes(N, K))
+
+
+def weight_bytes_compact(N: int, K: int) -> int:
+    return int(_lib.q4_weight_bytes_compact(N, K))
 
 
 def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
@@ -151,6 +164,32 @@ def unpack(qw: torch.Tensor, N: int, K: int, stream=None):
     return packed, scale, zero
 
 
+def repack_compact(packed: torch.Tensor, scale: torch.Tensor, zero: torch.Tensor, N: int, K: int,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Canonical arrays -> compact tiles (binary16 scales, 4-bit zeros)."""
+    for t, n in ((packed, "packed"), (scale, "scale"), (zero, "zero")):
+        _cuda(t, n)
+    nb = weight_bytes_compact(N, K)
+    if nb == 0:
+        raise ValueError(f"invalid shape {N}x{K}")
+    if out is None:
+        out = torch.empty(nb, dtype=torch.uint8, device=packed.device)
+    _ok(_lib.q4_repack_compact(packed.data_ptr(), scale.data_ptr(), zero.data_ptr(), N, K,
+                               out.data_ptr(), _stream(stream)), "q4_repack_compact")
+    return out
+
+
+def unpack_compact(qw: torch.Tensor, N: int, K: int, stream=None):
+    """Compact tiles -> (codes u8 [N][K/2], binary16 scale bits int16 [N][K/128], zeros u8 [N][K/128])."""
+    _cuda(qw, "qw")
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=qw.device)
+    scale16 = torch.empty((N, K // GROUP), dtype=torch.int16, device=qw.device)
+    zero = torch.empty((N, K // GROUP), dtype=torch.uint8, device=qw.device)
+    _ok(_lib.q4_unpack_compact(qw.data_ptr(), N, K, packed.data_ptr(), scale16.data_ptr(),
+                               zero.data_ptr(), _stream(stream)), "q4_unpack_compact")
+    return packed, scale16, zero
+
+
 def xsum(x: torch.Tensor, stream=None) -> torch.Tensor:
     _cuda(x, "x")
     M, K = x.shape
@@ -162,15 +201,20 @@ def xsum(x: torch.Tensor, stream=None) -> torch.Tensor:
 
 @dataclass
 class QWeight:
-    """A weight matrix in the tiled kernel layout."""
-    data: torch.Tensor  # uint8 [weight_bytes(N, K)]
+    """A weight matrix in the tiled kernel layout (compact: binary16 scales
+    and 4-bit zeros, GEMV only)."""
+    data: torch.Tensor  # uint8 [weight_bytes(N, K)] or [weight_bytes_compact(N, K)]
     N: int
     K: int
+    compact: bool = False
 
     @classmethod
-    def from_float(cls, w: torch.Tensor, stream=None, symmetric: bool = False) -> "QWeight":
+    def from_float(cls, w: torch.Tensor, stream=None, symmetric: bool = False,
+                   compact: bool = False) -> "QWeight":
         N, K = w.shape
         packed, scale, zero = quantize(w, stream, symmetric=symmetric)
+        if compact:
+            return cls(repack_compact(packed, scale, zero, N, K, stream=stream), N, K, True)
         return cls(repack(packed, scale, zero, N, K, stream=stream), N, K)
 
 
@@ -194,6 +238,13 @@ def gemv(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None 
     if ws is None:
         ws = workspace(M, qw.N, K, x.device)
     wsp, wsb = (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
+    if qw.compact:
+        if path != PATH_AUTO:
+            raise ValueError("compact weights run on the default (tensor-core) path only")
+        _ok(_lib.q4_gemv_compact(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
+                                 out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, _stream(stream)),
+            "q4_gemv_compact")
+        return out
     _ok(_lib.q4_gemv_path(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
                           out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, path, _stream(stream)),
         "q4_gemv")
@@ -213,6 +264,8 @@ def gemm(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None 
          stream=None) -> torch.Tensor:
     """Y [M][N] = X [M][K] * w_hat^T on the tcgen05 tensor cores (large M)."""
     _cuda(x, "x")
+    if qw.compact:
+        raise ValueError("q4_gemm reads the 1104-byte tile layout; compact weights are GEMV-only")
     M, K = x.shape
     if out is None:
         out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)

@@ -66,19 +66,19 @@ static inline bool sizes_ok(int64_t N, int64_t K)
 static q4_status gemv_common(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
                              const void *qw, void *y, q4_dtype yt, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream, int path,
-                             int debug_no_copy, uint64_t wait_ns)
+                             int debug_no_copy, uint64_t wait_ns, bool cmp = false)
 {
     if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
     if (!sizes_ok(N, K) || N > (1LL << 28)) return Q4_ERR_INVALID_ARG;
     if (M < 1 || M > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED;
     if (!valid_dtype(xt) || !valid_dtype(yt)) return Q4_ERR_UNSUPPORTED;
-    if (path == PATH_FMA && M != 1) return Q4_ERR_UNSUPPORTED;
+    if (path == PATH_FMA && (M != 1 || cmp)) return Q4_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(qw) || !aligned16(y) || !aligned16(workspace))
         return Q4_ERR_MISALIGNED;
     const DevInfo *d = dev_info();
     if (!d) return cuda_fail(cudaGetLastError());
     const GemvPlan plan = gemv_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                    xt, path, d->sm_count);
+                                    xt, path, d->sm_count, cmp);
     if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace))
         return Q4_ERR_INVALID_ARG;
     GemvArgs a{};
@@ -158,6 +158,35 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
 
+size_t q4_weight_bytes_compact(int64_t N, int64_t K)
+{
+    if (!sizes_ok(N, K)) return 0;
+    return static_cast<size_t>((N + TILE_ROWS - 1) / TILE_ROWS) * static_cast<size_t>(K / G) *
+           CMP_TILE_BYTES;
+}
+
+q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                            int64_t N, int64_t K, void *qw, q4_stream_t stream)
+{
+    if (!packed || !scale || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
+    if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
+    const cudaError_t e = repack_compact_launch(packed, scale, zero, N, K,
+                                                static_cast<uint8_t *>(qw),
+                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4_OK : cuda_fail(e);
+}
+
+q4_status q4_unpack_compact(const void *qw, int64_t N, int64_t K, uint8_t *packed,
+                            uint16_t *scale16, uint8_t *zero, q4_stream_t stream)
+{
+    if (!packed || !scale16 || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
+    if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
+    const cudaError_t e = unpack_compact_launch(static_cast<const uint8_t *>(qw), N, K, packed,
+                                                scale16, zero,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q4_OK : cuda_fail(e);
+}
+
 q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
                   q4_stream_t stream)
 {
@@ -177,13 +206,14 @@ size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K)
     size_t need = 0;
     const q4_dtype types[3] = {Q4_BF16, Q4_F16, Q4_F32};
     const int paths[3] = {PATH_AUTO, PATH_MMA, PATH_FMA};
-    for (q4_dtype t : types)
-        for (int p : paths) {
-            if (p == PATH_FMA && M != 1) continue;
-            const GemvPlan g = gemv_plan(static_cast<int>(M), static_cast<int>(N),
-                                         static_cast<int>(K), t, p, d->sm_count);
-            need = std::max(need, g.workspace);
-        }
+    for (int cmp = 0; cmp < 2; ++cmp)
+        for (q4_dtype t : types)
+            for (int p : paths) {
+                if (p == PATH_FMA && (M != 1 || cmp)) continue;
+                const GemvPlan g = gemv_plan(static_cast<int>(M), static_cast<int>(N),
+                                             static_cast<int>(K), t, p, d->sm_count, cmp != 0);
+                need = std::max(need, g.workspace);
+            }
     return need;
 }
 
@@ -193,6 +223,14 @@ q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
 {
     return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 0, 1000000000ull);
+}
+
+q4_status q4_gemv_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                          const void *qw, void *y, q4_dtype yt, void *workspace,
+                          size_t workspace_bytes, q4_stream_t stream)
+{
+    return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 0, 1000000000ull, true);
 }
 
 q4_status q4_gemv_path(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,

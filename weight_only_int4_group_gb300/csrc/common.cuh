@@ -24,6 +24,11 @@ constexpr int TILE_BYTES = Q4_TILE_BYTES;   // 1104
 constexpr int CODE_BYTES = 1024;            // 16 rows x 128 codes / 2
 constexpr int SCALE_OFF = 1024;             // 8 pairs of f32 scales
 constexpr int ZERO_OFF = 1088;              // 8 pairs of u8 zeros
+// Compact tiles: the same codes, then 8 pairs of binary16 scales (bytes
+// 1024..1055), 8 bytes of zero-nibble pairs (z_i | z_{i+8} << 4), 8 bytes of
+// padding: 1072 = 67 x 16 bytes, so every tile stays 16-byte aligned.
+constexpr int CMP_TILE_BYTES = Q4_CMP_TILE_BYTES;  // 1072
+constexpr int CMP_ZERO_OFF = 1056;
 
 // Device error word (one per device, defined in api.cu, its address passed to
 // every kernel that waits): bit 0 = a bounded wait timed out.  Read and
@@ -230,10 +235,11 @@ struct GemvPlan {
     int maxc;  // most CTAs sharing one row block (1: no partial sums)
     bool deep; // 3-stage ring (M = 1, 16-bit activations, many steps per CTA)
     bool small;  // 2-tile row blocks (few steps per CTA)
+    bool cmp;    // compact tiles (binary16 scales, 4-bit zeros)
     size_t workspace;
 };
 
-GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
+GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count, bool cmp = false);
 // Counter block at the start of the workspace: one u32 arrival counter per
 // 32 output rows (at least one per row block), padded to 256 bytes.
 size_t gemv_counter_bytes(int64_t N);
@@ -245,6 +251,10 @@ cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8
                           int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
 cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
                           uint8_t *zero, cudaStream_t s);
+cudaError_t repack_compact_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                                  int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
+cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed,
+                                  uint16_t *scale16, uint8_t *zero, cudaStream_t s);
 q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                    void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
                    cudaError_t *cerr);

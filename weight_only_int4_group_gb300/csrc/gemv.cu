@@ -77,17 +77,18 @@ constexpr int MIN_BLOCKS = 2;  // CTAs per SM the shared memory budget is sized 
 
 constexpr int XROW = W * G * 2 + 16;  // MMA staged activations: one padded row per batch row
 
-// xrows: batch rows staged with each step (MMA, M <= 8); 0 otherwise
-__host__ __device__ constexpr int stage_bytes(int mode, int xrows, int rb = RB)
+// xrows: batch rows staged with each step (MMA, M <= 8); 0 otherwise;
+// tb: bytes per tile (TILE_BYTES, or CMP_TILE_BYTES for compact metadata)
+__host__ __device__ constexpr int stage_bytes(int mode, int xrows, int rb = RB, int tb = TILE_BYTES)
 {
-    return mode == PATH_FMA ? rb * W * TILE_BYTES + XSTAGE_BYTES
-                            : ((rb * W * TILE_BYTES + xrows * XROW + 127) / 128) * 128;
+    return mode == PATH_FMA ? rb * W * tb + XSTAGE_BYTES
+                            : ((rb * W * tb + xrows * XROW + 127) / 128) * 128;
 }
 
 __host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms, int nstage = NSTAGE,
-                                             int rb = RB)
+                                             int rb = RB, int tb = TILE_BYTES)
 {
-    return nstage * stage_bytes(mode, xrows, rb) + CTRL_BYTES +
+    return nstage * stage_bytes(mode, xrows, rb, tb) + CTRL_BYTES +
            (mode == PATH_FMA ? (W * WARP_PAIR_FLOATS + W * rb * 16) * 4 : W * rb * 16 * ms * 4) +
            rb * 16 * ms * 4;  // hand-off buffer of one row block
 }
@@ -218,21 +219,40 @@ __host__ __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64
     return ((i + 1) * G - 1) / T;
 }
 
+// Scale and zero pairs (rows i and i + 8 of a tile, i = gq) of one tile:
+// f32 scales and u8 zeros, or (compact) binary16 scales and one byte of two
+// zero nibbles; the zeros come back as z_i | z_{i+8} << 8 either way.
+template <bool CMP>
+__device__ __forceinline__ void tile_meta(const uint8_t *tile, int gq, float2 &sp, uint32_t &zp)
+{
+    if (CMP) {
+        sp = __half22float2(*reinterpret_cast<const __half2 *>(tile + SCALE_OFF + 4 * gq));
+        const uint32_t b = tile[CMP_ZERO_OFF + gq];
+        zp = (b & 0x0Fu) | ((b >> 4) << 8);
+    } else {
+        sp = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
+        zp = *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq);
+    }
+}
+
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
 // XSPLIT: f32 activations carried as bf16 hi + bf16 lo (two MMAs per step).
 // ONE: M = 1 known at compile time (unused MMA columns skipped).
 // RBT: row tiles per row block.
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE, int RBT>
+// CMP: compact tiles (binary16 scales, 4-bit zeros; tensor-core path only).
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE, int RBT, bool CMP>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
     constexpr int RB = RBT;
-    constexpr int TILES_BYTES = RBT * W * TILE_BYTES;
+    constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
+    static_assert(!(CMP && MODE == PATH_FMA), "compact tiles: tensor-core path only");
+    constexpr int TILES_BYTES = RBT * W * TBY;
     constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     // XS32: M = 1 f32 activations staged as f32 with the tiles (split into
     // bf16 hi + lo per step); the FMA path stages the same way
     constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
     const int xrows = XSTAGED ? (ONE ? 1 : a.M) : 0;
-    const int SB = stage_bytes(XS32 ? PATH_FMA : MODE, xrows, RBT);
+    const int SB = stage_bytes(XS32 ? PATH_FMA : MODE, xrows, RBT, TBY);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTG * SB);
@@ -306,14 +326,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                         break;
                     const int rt0 = rb * RB, nrt = min(RB, ntiles - rt0);
                     const int g0 = s * W, ng = min(W, NG - g0);
-                    const uint32_t row_bytes = static_cast<uint32_t>(ng) * TILE_BYTES;
+                    const uint32_t row_bytes = static_cast<uint32_t>(ng) * TBY;
                     const uint32_t xbytes = (MODE == PATH_FMA || XS32) ? static_cast<uint32_t>(ng) * G * xb
                                             : static_cast<uint32_t>(xrows) * ng * G * 2;
                     uint8_t *stage = ring + slot * SB;
                     mbar_arrive_expect_tx(&full[slot], row_bytes * nrt + xbytes);
                     for (int r = 0; r < nrt; ++r)
-                        bulk_g2s(stage + r * W * TILE_BYTES,
-                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g0) * TILE_BYTES,
+                        bulk_g2s(stage + r * W * TBY,
+                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g0) * TBY,
                                  row_bytes, &full[slot]);
                     if (gstep < npro) {
                         pro_g0[gstep] = g0;
@@ -493,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             load_b((s + 1 == NS ? 0 : s + 1) * W + warp,
                    reinterpret_cast<uint32_t (&)[NT][8][2]>(bnxt), blo);
         const uint8_t *stage = ring + slot * SB;
-        const uint8_t *wtiles = stage + warp * TILE_BYTES;
+        const uint8_t *wtiles = stage + warp * TBY;
         if (XS32) {
             // B fragments (k = 16j + 2t + {0, 1} and + 8) of the single
             // activation row, each f32 pair split into bf16 hi + bf16 lo
@@ -568,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             uint32_t zp[RB];
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
-                const uint8_t *tile = wtiles + r * W * TILE_BYTES;
+                const uint8_t *tile = wtiles + r * W * TBY;
                 const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
                 const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
                 sp[r] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
@@ -621,11 +641,10 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 uint32_t zp[TI];
 #pragma unroll
                 for (int i = 0; i < TI; ++i) {
-                    const uint8_t *tile = wtiles + (r0 + i) * W * TILE_BYTES;
+                    const uint8_t *tile = wtiles + (r0 + i) * W * TBY;
                     const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
                     const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
-                    sp[i] = *reinterpret_cast<const float2 *>(tile + SCALE_OFF + 8 * gq);
-                    zp[i] = *reinterpret_cast<const uint16_t *>(tile + ZERO_OFF + 2 * gq);
+                    tile_meta<CMP>(tile, gq, sp[i], zp[i]);
                     wv[i][0] = c0.x; wv[i][1] = c0.y; wv[i][2] = c0.z; wv[i][3] = c0.w;
                     wv[i][4] = c1.x; wv[i][5] = c1.y; wv[i][6] = c1.z; wv[i][7] = c1.w;
                 }
@@ -754,15 +773,18 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 }
 
 // -------------------------------------------------------------------- host
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false, int RBT = RB>
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false, int RBT = RB,
+          bool CMP = false>
 struct Kern {
     static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
     static constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
+    static constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     static int smem(int M)
     {
         if (XS32)  // f32 staging as in the FMA path, MMA-sized reduction buffers
-            return NSTG * stage_bytes(PATH_FMA, 0, RBT) + CTRL_BYTES + W * RBT * 16 * 4 + RBT * 16 * 4;
-        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG, RBT);
+            return NSTG * stage_bytes(PATH_FMA, 0, RBT, TBY) + CTRL_BYTES + W * RBT * 16 * 4 +
+                   RBT * 16 * 4;
+        return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG, RBT, TBY);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
     {
@@ -776,7 +798,7 @@ struct Kern {
             *blocks_per_sm = known;
             return cudaSuccess;
         }
-        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT>;
+        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP>;
         if (!attr[dev].load(std::memory_order_relaxed)) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem(NSTG == NSTAGE ? 16 : 1));
@@ -803,34 +825,49 @@ struct Kern {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT>, a);
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP>, a);
     }
 };
 
-template <typename F>
-static cudaError_t dispatch(int path, int M, q4_dtype xt, bool deep, bool small, F &&f)
+template <bool CMP, typename F>
+static cudaError_t dispatch_t(int path, int M, q4_dtype xt, bool deep, bool small, F &&f)
 {
-    if (path == PATH_FMA) return f(Kern<PATH_FMA, 1, 0, false>{});
+    if (path == PATH_FMA) {
+        if constexpr (CMP) return cudaErrorInvalidValue;  // rejected before planning
+        else return f(Kern<PATH_FMA, 1, 0, false>{});
+    }
     // small: 2-tile row blocks (2 <= M <= 8, 16-bit activations staged)
     if (small && M >= 2 && M <= 8 && xt != Q4_F32) {
-        if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL>{});
-        return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL>{});
+        if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL, CMP>{});
+        return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL, CMP>{});
     }
     // deep: M = 1, where a 3-stage ring still fits two CTAs per SM
     const bool two = M > 8;
     if (xt == Q4_F16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3, true>{});
-        if (M == 1) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, true>{});
-        return two ? f(Kern<PATH_MMA, 2, 1, false>{}) : f(Kern<PATH_MMA, 1, 1, false>{});
+        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3, true, RB, CMP>{});
+        if (M == 1) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, true, RB, CMP>{});
+        return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB, CMP>{})
+                   : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB, CMP>{});
     }
     if (xt == Q4_BF16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3, true>{});
-        if (M == 1) return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true>{});
-        return two ? f(Kern<PATH_MMA, 2, 0, false>{}) : f(Kern<PATH_MMA, 1, 0, false>{});
+        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3, true, RB, CMP>{});
+        if (M == 1) return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true, RB, CMP>{});
+        return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB, CMP>{})
+                   : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB, CMP>{});
     }
     if (M == 1)
-        return deep ? f(Kern<PATH_MMA, 1, 0, true, 3, true>{}) : f(Kern<PATH_MMA, 1, 0, true, NSTAGE, true>{});
-    return two ? f(Kern<PATH_MMA, 2, 0, true>{}) : f(Kern<PATH_MMA, 1, 0, true>{});
+        return deep ? f(Kern<PATH_MMA, 1, 0, true, 3, true, RB, CMP>{})
+                    : f(Kern<PATH_MMA, 1, 0, true, NSTAGE, true, RB, CMP>{});
+    return two ? f(Kern<PATH_MMA, 2, 0, true, NSTAGE, false, RB, CMP>{})
+               : f(Kern<PATH_MMA, 1, 0, true, NSTAGE, false, RB, CMP>{});
+}
+
+// cmp: compact tiles (binary16 scales, 4-bit zeros)
+template <typename F>
+static cudaError_t dispatch(bool cmp, int path, int M, q4_dtype xt, bool deep, bool small, F &&f)
+{
+    return cmp ? dispatch_t<true>(path, M, xt, deep, small, f)
+               : dispatch_t<false>(path, M, xt, deep, small, f);
 }
 
 size_t gemv_counter_bytes(int64_t N)
@@ -838,26 +875,26 @@ size_t gemv_counter_bytes(int64_t N)
     return ((static_cast<size_t>((N + 31) / 32) * sizeof(unsigned int) + 255) / 256) * 256;
 }
 
-static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count);
+static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count, bool cmp);
 
-// Plans depend only on (device, shape, activation type, path); a decode loop
-// asks for the same few again and again, so they are kept (a small map,
-// cleared if it ever grows large).
-GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
+// Plans depend only on (device, shape, activation type, path, tile layout);
+// a decode loop asks for the same few again and again, so they are kept (a
+// small map, cleared if it ever grows large).
+GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count, bool cmp)
 {
     struct Key {
-        int dev, M, N, K, xt, path, sms;
+        int dev, M, N, K, xt, path, sms, cmp;
         bool operator==(const Key &o) const
         {
             return dev == o.dev && M == o.M && N == o.N && K == o.K && xt == o.xt &&
-                   path == o.path && sms == o.sms;
+                   path == o.path && sms == o.sms && cmp == o.cmp;
         }
     };
     struct Hash {
         size_t operator()(const Key &k) const
         {
             uint64_t h = 1469598103934665603ull;
-            for (int v : {k.dev, k.M, k.N, k.K, k.xt, k.path, k.sms})
+            for (int v : {k.dev, k.M, k.N, k.K, k.xt, k.path, k.sms, k.cmp})
                 h = (h ^ static_cast<uint32_t>(v)) * 1099511628211ull;
             return static_cast<size_t>(h);
         }
@@ -866,13 +903,13 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     static std::unordered_map<Key, GemvPlan, Hash> plans;
     int dev = 0;
     cudaGetDevice(&dev);
-    const Key key{dev, M, N, K, static_cast<int>(xt), path, sm_count};
+    const Key key{dev, M, N, K, static_cast<int>(xt), path, sm_count, cmp ? 1 : 0};
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = plans.find(key);
         if (it != plans.end()) return it->second;
     }
-    const GemvPlan p = make_plan(M, N, K, xt, path, sm_count);
+    const GemvPlan p = make_plan(M, N, K, xt, path, sm_count, cmp);
     if (p.grid > 0) {  // a plan whose kernel configuration failed is not kept
         std::lock_guard<std::mutex> lock(mu);
         if (plans.size() > 4096) plans.clear();
@@ -881,9 +918,10 @@ GemvPlan gemv_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
     return p;
 }
 
-static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count)
+static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_count, bool cmp)
 {
     GemvPlan p{};
+    p.cmp = cmp;
     // AUTO: the tensor-core path (its unpack costs 7 ALU instructions per 8
     // weights against 11 for the CUDA-core path, which is bound by the ALU
     // pipe); f32 activations ride as bf16 hi + lo with two MMAs per word,
@@ -896,7 +934,7 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     const int NS = (NG + W - 1) / W;
     int dev = 0, per_sm = 1;
     cudaGetDevice(&dev);
-    cudaError_t cfg = dispatch(path, M, xt, false, false,
+    cudaError_t cfg = dispatch(cmp, path, M, xt, false, false,
                                [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
     // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 8: use
     // 2-tile ones, so that steps are short and plentiful (measured faster
@@ -905,7 +943,7 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     p.small = T8 < 4 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 2 &&
               M <= 8 && xt != Q4_F32;
     if (p.small && cfg == cudaSuccess)
-        cfg = dispatch(path, M, xt, false, true,
+        cfg = dispatch(cmp, path, M, xt, false, true,
                        [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
     p.rb = p.small ? RB_SMALL : RB;
     p.nrb = (ntiles + p.rb - 1) / p.rb;
@@ -924,7 +962,7 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     p.deep = !p.small && path == PATH_MMA && M == 1 && T >= 5 * static_cast<int64_t>(p.grid);
     if (p.deep) {  // same CTAs per SM, or keep the 2-stage ring
         int per_sm_deep = 0;
-        dispatch(path, M, xt, true, false,
+        dispatch(cmp, path, M, xt, true, false,
                  [&](auto k) { return decltype(k)::configure(dev, M, &per_sm_deep); });
         p.deep = per_sm_deep == per_sm;
     }
@@ -944,7 +982,7 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
 
 cudaError_t gemv_launch(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
 {
-    return dispatch(p.path, a.M, a.xt, p.deep, p.small,
+    return dispatch(p.cmp, p.path, a.M, a.xt, p.deep, p.small,
                     [&](auto k) { return decltype(k)::launch(p.grid, a, s); });
 }
 

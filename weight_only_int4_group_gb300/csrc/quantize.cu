@@ -182,6 +182,27 @@ __device__ __forceinline__ uint32_t interleave4(uint32_t b0, uint32_t b1, uint32
     return lo | (hi << 16);
 }
 
+// Code chunk `unit` (0..63) of tile (row0, g): 16 bytes, lane l = unit % 32,
+// chunk c = unit / 32 (see the word layout above).
+__device__ __forceinline__ uint4 code_chunk(const uint8_t *__restrict__ packed, int N, int K,
+                                            int64_t row0, int g, int unit)
+{
+    const int c = unit >> 5, l = unit & 31;
+    const int r = l >> 2, t = l & 3;
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = 4 * c + i;
+        const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;  // even k
+        auto byte_at = [&](int64_t row, int64_t k) -> uint32_t {
+            return row < N ? packed[row * (K / 2) + k / 2] : 0u;
+        };
+        out[i] = interleave4(byte_at(row0 + r, kb), byte_at(row0 + r + 8, kb),
+                             byte_at(row0 + r + 8, kb + 8), byte_at(row0 + r, kb + 8));
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // 69 sixteen-byte units per tile: 64 code chunks, 4 scale units, 1 zero unit.
 __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
                          const uint8_t *__restrict__ zero, int N, int K, int64_t ntiles_total,
@@ -198,21 +219,7 @@ __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__rest
         const int64_t row0 = rt * TILE_ROWS;
         uint8_t *dst = qw + tile * TILE_BYTES;
         if (unit < 64) {
-            const int c = unit >> 5, l = unit & 31;
-            const int r = l >> 2, t = l & 3;
-            uint32_t out[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 4 * c + i;
-                const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;  // even k
-                auto byte_at = [&](int64_t row, int64_t k) -> uint32_t {
-                    return row < N ? packed[row * (K / 2) + k / 2] : 0u;
-                };
-                out[i] = interleave4(byte_at(row0 + r, kb), byte_at(row0 + r + 8, kb),
-                                     byte_at(row0 + r + 8, kb + 8), byte_at(row0 + r, kb + 8));
-            }
-            *reinterpret_cast<uint4 *>(dst + (c * 32 + l) * 16) =
-                make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4 *>(dst + unit * 16) = code_chunk(packed, N, K, row0, g, unit);
         } else if (unit < 68) {
             float sv[4];
 #pragma unroll
@@ -237,6 +244,71 @@ __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__rest
     }
 }
 
+// Compact tiles: 67 sixteen-byte units per tile: 64 code chunks, 2 units of
+// binary16 scale pairs (each scale rounded to nearest even), 1 unit of 8
+// zero-nibble pairs and 8 bytes of padding.
+__global__ void k_repack_compact(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
+                                 const uint8_t *__restrict__ zero, int N, int K, int64_t ntiles_total,
+                                 uint8_t *__restrict__ qw)
+{
+    const int NG = K / G;
+    const int64_t units = ntiles_total * 67;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = u / 67;
+        const int unit = static_cast<int>(u % 67);
+        const int64_t rt = tile / NG;
+        const int g = static_cast<int>(tile % NG);
+        const int64_t row0 = rt * TILE_ROWS;
+        uint8_t *dst = qw + tile * CMP_TILE_BYTES;
+        if (unit < 64) {
+            *reinterpret_cast<uint4 *>(dst + unit * 16) = code_chunk(packed, N, K, row0, g, unit);
+        } else if (unit < 66) {
+            uint32_t hw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {  // pair 4 (unit - 64) + e: rows pair, pair + 8
+                const int pair = 4 * (unit - 64) + e;
+                const int64_t r0 = row0 + pair, r8 = r0 + 8;
+                const __half h0 = __float2half_rn(r0 < N ? scale[r0 * NG + g] : 0.0f);
+                const __half h8 = __float2half_rn(r8 < N ? scale[r8 * NG + g] : 0.0f);
+                hw[e] = static_cast<uint32_t>(__half_as_ushort(h0)) |
+                        (static_cast<uint32_t>(__half_as_ushort(h8)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(dst + SCALE_OFF + (unit - 64) * 16) =
+                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        } else {
+            uint32_t zw[2] = {0, 0};
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {  // pair b: rows b (low nibble), b + 8 (high)
+                const int64_t r0 = row0 + b, r8 = r0 + 8;
+                const uint32_t z0 = r0 < N ? (zero[r0 * NG + g] & 15u) : 0u;
+                const uint32_t z8 = r8 < N ? (zero[r8 * NG + g] & 15u) : 0u;
+                zw[b >> 2] |= (z0 | (z8 << 4)) << ((b & 3) * 8);
+            }
+            *reinterpret_cast<uint4 *>(dst + CMP_ZERO_OFF) = make_uint4(zw[0], zw[1], 0u, 0u);
+        }
+    }
+}
+
+// Code word i of chunk c of lane l of tile (row0, g) back into the
+// canonical bytes (rows past N are dropped).
+__device__ __forceinline__ void put_code_word(uint8_t *__restrict__ packed, int N, int K,
+                                              int64_t row0, int g, int c, int l, int i, uint32_t w)
+{
+    const int r = l >> 2, t = l & 3, j = 4 * c + i;
+    const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;
+    auto put = [&](int64_t row, int64_t k, int f) {
+        if (row < N) {
+            const uint32_t lo = (w >> (4 * f)) & 15u, hi = (w >> (16 + 4 * f)) & 15u;
+            packed[row * (K / 2) + k / 2] = static_cast<uint8_t>(lo | (hi << 4));
+        }
+    };
+    put(row0 + r, kb, 0);
+    put(row0 + r + 8, kb, 1);
+    put(row0 + r + 8, kb + 8, 2);
+    put(row0 + r, kb + 8, 3);
+}
+
 // Inverse: one thread per code word (4 canonical bytes), plus one per tile
 // row-pair for the metadata.
 __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t ntiles_total,
@@ -255,19 +327,8 @@ __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t n
         const uint8_t *src = qw + tile * TILE_BYTES;
         if (unit < 256) {
             const int c = unit >> 7, l = (unit >> 2) & 31, i = unit & 3;
-            const int r = l >> 2, t = l & 3, j = 4 * c + i;
             const uint32_t w = reinterpret_cast<const uint32_t *>(src)[(c * 32 + l) * 4 + i];
-            const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;
-            auto put = [&](int64_t row, int64_t k, int f) {
-                if (row < N) {
-                    const uint32_t lo = (w >> (4 * f)) & 15u, hi = (w >> (16 + 4 * f)) & 15u;
-                    packed[row * (K / 2) + k / 2] = static_cast<uint8_t>(lo | (hi << 4));
-                }
-            };
-            put(row0 + r, kb, 0);
-            put(row0 + r + 8, kb, 1);
-            put(row0 + r + 8, kb + 8, 2);
-            put(row0 + r, kb + 8, 3);
+            put_code_word(packed, N, K, row0, g, c, l, i, w);
         } else {
             const int pair = unit - 256;
             const float *sp = reinterpret_cast<const float *>(src + SCALE_OFF) + 2 * pair;
@@ -279,6 +340,42 @@ __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t n
             if (row0 + pair + 8 < N) {
                 scale[(row0 + pair + 8) * NG + g] = sp[1];
                 zero[(row0 + pair + 8) * NG + g] = zp[1];
+            }
+        }
+    }
+}
+
+// Inverse of the compact layout: codes, binary16 scale bits, one zero byte
+// per group.
+__global__ void k_unpack_compact(const uint8_t *__restrict__ qw, int N, int K, int64_t ntiles_total,
+                                 uint8_t *__restrict__ packed, uint16_t *__restrict__ scale16,
+                                 uint8_t *__restrict__ zero)
+{
+    const int NG = K / G;
+    const int64_t units = ntiles_total * (256 + 8);
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = u / 264;
+        const int unit = static_cast<int>(u % 264);
+        const int64_t rt = tile / NG;
+        const int g = static_cast<int>(tile % NG);
+        const int64_t row0 = rt * TILE_ROWS;
+        const uint8_t *src = qw + tile * CMP_TILE_BYTES;
+        if (unit < 256) {
+            const int c = unit >> 7, l = (unit >> 2) & 31, i = unit & 3;
+            const uint32_t w = reinterpret_cast<const uint32_t *>(src)[(c * 32 + l) * 4 + i];
+            put_code_word(packed, N, K, row0, g, c, l, i, w);
+        } else {
+            const int pair = unit - 256;
+            const uint16_t *sp = reinterpret_cast<const uint16_t *>(src + SCALE_OFF) + 2 * pair;
+            const uint32_t zb = src[CMP_ZERO_OFF + pair];
+            if (row0 + pair < N) {
+                scale16[(row0 + pair) * NG + g] = sp[0];
+                zero[(row0 + pair) * NG + g] = static_cast<uint8_t>(zb & 15u);
+            }
+            if (row0 + pair + 8 < N) {
+                scale16[(row0 + pair + 8) * NG + g] = sp[1];
+                zero[(row0 + pair + 8) * NG + g] = static_cast<uint8_t>(zb >> 4);
             }
         }
     }
@@ -340,6 +437,24 @@ cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *pack
     k_unpack<<<grid_for(ntiles * 264, 256), 256, 0, s>>>(qw, static_cast<int>(N),
                                                          static_cast<int>(K), ntiles, packed,
                                                          scale, zero);
+    return cudaGetLastError();
+}
+
+cudaError_t repack_compact_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
+                                  int64_t N, int64_t K, uint8_t *qw, cudaStream_t s)
+{
+    const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
+    k_repack_compact<<<grid_for(ntiles * 67, 256), 256, 0, s>>>(
+        packed, scale, zero, static_cast<int>(N), static_cast<int>(K), ntiles, qw);
+    return cudaGetLastError();
+}
+
+cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed,
+                                  uint16_t *scale16, uint8_t *zero, cudaStream_t s)
+{
+    const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
+    k_unpack_compact<<<grid_for(ntiles * 264, 256), 256, 0, s>>>(
+        qw, static_cast<int>(N), static_cast<int>(K), ntiles, packed, scale16, zero);
     return cudaGetLastError();
 }
 
