@@ -53,6 +53,11 @@
 //     lane loads its B fragments from L2 one step ahead.  The group sums of the
 //     activations come from one extra MMA per k-step with an all-ones A
 //     operand.  Per group, y += scale * (D - (offset + zero) * sum x).
+//
+// Both consumers read 1104-byte tiles (f32 scales, u8 zeros); the tensor-core
+// one also reads compact 1072-byte tiles (binary16 scales widened exactly,
+// zero nibbles; the format the page "Weight quantization" counts as 16-bit
+// scales and 4-bit zeros), selected at compile time.
 #include <mutex>
 #include <unordered_map>
 
