@@ -142,9 +142,10 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
  *   scale16 [N][K/128], zeros [N][K/128] (one byte per group).
  * q4_gemv_compact: q4_gemv on compact tiles (tensor-core path; same
  *   arguments, workspace and errors; q4_gemv_workspace_bytes covers it).
- * The layout of qw is not recorded in the buffer: compact tiles go to
- * q4_gemv_compact only (q4_gemv, q4_gemv_path and q4_gemm read 1104-byte
- * tiles and would read past the end of a compact buffer).
+ * q4_gemm_compact: q4_gemm on compact tiles (same arguments and errors).
+ * The layout of qw is not recorded in the buffer: compact tiles go to the
+ * _compact entry points only (q4_gemv, q4_gemv_path and q4_gemm read
+ * 1104-byte tiles and would read past the end of a compact buffer).
  */
 size_t q4_weight_bytes_compact(int64_t N, int64_t K);
 q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uint8_t *zero,
@@ -154,6 +155,8 @@ q4_status q4_unpack_compact(const void *qw, int64_t N, int64_t K, uint8_t *packe
 q4_status q4_gemv_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
                           const void *qw, void *y, q4_dtype yt, void *workspace,
                           size_t workspace_bytes, q4_stream_t stream);
+q4_status q4_gemm_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream);
 
 /*
  * Activation group sums, xsum[m][g] = sum_{k in group g} x[m][k] accumulated

@@ -81,12 +81,25 @@ def test_gemv_compact_many_steps_per_cta():
     compare(y, yr, ar, where="compact gemv long K")
 
 
-def test_compact_rejected_by_other_products():
+@pytest.mark.parametrize("M,N,K,xdt", [(300, 384, 1024, torch.bfloat16), (17, 160, 2048, torch.float16),
+                                       (64, 256, 384, torch.bfloat16)])
+def test_gemm_compact_parity(M, N, K, xdt):
+    import weight_only_int4_group_gb300 as q4
+    W = synth.normal_rows(M + N, K, 0, N, 0.02)
+    x, xf = x_for(xdt, M, K, seed=M + 5)
+    qw = q4.QWeight.from_float(dev_f32(W), compact=True)
+    y = q4.gemm(x, qw, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert q4.check() == q4.OK
+    p, _, z, se = _oracle_compact(W)
+    yr, ar = oracle.load().dot_naive(xf, p, se, z, N, K, threads=8)
+    compare(y, yr, ar, where=f"compact gemm {M}x{N}x{K}")
+
+
+def test_compact_rejected_by_the_cuda_core_path():
     import weight_only_int4_group_gb300 as q4
     qw = q4.QWeight.from_float(dev_f32(np.zeros((32, 128), np.float32)), compact=True)
-    x = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError):
-        q4.gemm(x, qw)
+    x = torch.zeros((1, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         q4.gemv(x, qw, path=q4.PATH_FMA)
 

@@ -59,6 +59,7 @@ def _load():
     lib.q4_repack_compact.argtypes = [P, P, P, I, I, P, P]
     lib.q4_unpack_compact.argtypes = [P, I, I, P, P, P, P]
     lib.q4_gemv_compact.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
+    lib.q4_gemm_compact.argtypes = [P, S, I, I, I, P, P, S, P]
     lib.q4_xsum.argtypes = [P, S, I, I, P, P]
     lib.q4_gemv_workspace_bytes.argtypes = [I, I, I]
     lib.q4_gemv_workspace_bytes.restype = Z
@@ -71,7 +72,7 @@ def _load():
     lib.q4_status_str.restype = ctypes.c_char_p
     lib.q4_last_cuda_error.restype = ctypes.c_char_p
     for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_repack_compact",
-              "q4_unpack_compact", "q4_gemv_compact", "q4_xsum", "q4_gemv", "q4_gemv_path",
+              "q4_unpack_compact", "q4_gemv_compact", "q4_gemm_compact", "q4_xsum", "q4_gemv", "q4_gemv_path",
               "q4_gemv_timeout_selftest", "q4_gemm", "q4_check"):
         getattr(lib, f).restype = S
     return lib
@@ -202,7 +203,7 @@ def xsum(x: torch.Tensor, stream=None) -> torch.Tensor:
 @dataclass
 class QWeight:
     """A weight matrix in the tiled kernel layout (compact: binary16 scales
-    and 4-bit zeros, GEMV only)."""
+    and 4-bit zeros)."""
     data: torch.Tensor  # uint8 [weight_bytes(N, K)] or [weight_bytes_compact(N, K)]
     N: int
     K: int
@@ -264,13 +265,12 @@ def gemm(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None 
          stream=None) -> torch.Tensor:
     """Y [M][N] = X [M][K] * w_hat^T on the tcgen05 tensor cores (large M)."""
     _cuda(x, "x")
-    if qw.compact:
-        raise ValueError("q4_gemm reads the 1104-byte tile layout; compact weights are GEMV-only")
     M, K = x.shape
     if out is None:
         out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)
-    _ok(_lib.q4_gemm(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
-                     out.data_ptr(), _DTYPE[out.dtype], _stream(stream)), "q4_gemm")
+    fn, name = (_lib.q4_gemm_compact, "q4_gemm_compact") if qw.compact else (_lib.q4_gemm, "q4_gemm")
+    _ok(fn(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(), out.data_ptr(),
+           _DTYPE[out.dtype], _stream(stream)), name)
     return out
 
 

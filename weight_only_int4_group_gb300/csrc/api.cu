@@ -250,8 +250,8 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
                        reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 1, 20000000ull);
 }
 
-q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                  void *y, q4_dtype yt, q4_stream_t stream)
+static q4_status gemm_common(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                             const void *qw, void *y, q4_dtype yt, q4_stream_t stream, bool cmp)
 {
     if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
     if (M < 1 || M > (1LL << 30) || !sizes_ok(N, K) || N % 16 != 0 || N > (1LL << 30))
@@ -263,9 +263,21 @@ q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
     if (!d) return cuda_fail(cudaGetLastError());
     cudaError_t e = cudaSuccess;
     const q4_status st = gemm_run(x, xt, M, N, K, qw, y, yt, d->sm_count, d->err,
-                                  reinterpret_cast<cudaStream_t>(stream), &e);
+                                  reinterpret_cast<cudaStream_t>(stream), &e, cmp);
     if (st == Q4_ERR_CUDA) return cuda_fail(e);
     return st;
+}
+
+q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
+                  void *y, q4_dtype yt, q4_stream_t stream)
+{
+    return gemm_common(x, xt, M, N, K, qw, y, yt, stream, false);
+}
+
+q4_status q4_gemm_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream)
+{
+    return gemm_common(x, xt, M, N, K, qw, y, yt, stream, true);
 }
 
 q4_status q4_check(q4_stream_t stream)

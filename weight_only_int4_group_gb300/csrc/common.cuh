@@ -257,7 +257,7 @@ cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8
                                   uint16_t *scale16, uint8_t *zero, cudaStream_t s);
 q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                    void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
-                   cudaError_t *cerr);
+                   cudaError_t *cerr, bool cmp = false);
 cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
                         cudaStream_t s);
 

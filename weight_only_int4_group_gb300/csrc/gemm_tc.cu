@@ -187,11 +187,13 @@ struct Args {
 
 // F16: activations (and the dequantized weights) are f16, else bf16.
 // YF16: outputs are f16, else bf16.  NARROW: the shared-memory plan for
-// token tiles of at most 64 rows.
-template <bool F16, bool YF16, bool NARROW>
+// token tiles of at most 64 rows.  CMP: compact tiles (binary16 scale
+// pairs, zero nibbles, 1072 bytes; a code stage still fits 8 of them).
+template <bool F16, bool YF16, bool NARROW, bool CMP>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmx, const Args a)
 {
+    constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     using P = Plan<NARROW>;
     constexpr int NS = P::NS, NC = P::NC, A_HALF = P::A_HALF, A_ST = P::A_ST, B_ST = P::B_ST;
     extern __shared__ uint8_t smem_raw[];
@@ -281,11 +283,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TILE_BYTES);
+                    mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TBY);
                     for (int r = 0; r < nrt; ++r)
-                        bulk_g2s(sC + sc * C_STAGE + r * TILE_BYTES,
-                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TILE_BYTES,
-                                 TILE_BYTES, &full_c[sc]);
+                        bulk_g2s(sC + sc * C_STAGE + r * TBY,
+                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TBY, TBY,
+                                 &full_c[sc]);
                     ++ic;
                 }
             }
@@ -359,11 +361,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 if (d < nrt) {
-                    const uint8_t *ct = sC + sc * C_STAGE + d * TILE_BYTES;
-                    const float2 sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
-                    const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
-                    const float nz0 = -(128.0f + static_cast<float>(zp & 0xFFu));
-                    const float nz8 = -(128.0f + static_cast<float>(zp >> 8));
+                    const uint8_t *ct = sC + sc * C_STAGE + d * TBY;
+                    float2 sp;
+                    uint32_t z0, z8;
+                    if (CMP) {  // binary16 pair (widened exactly), zero nibbles
+                        sp = __half22float2(*reinterpret_cast<const __half2 *>(ct + SCALE_OFF + 4 * gq));
+                        const uint32_t zb = ct[CMP_ZERO_OFF + gq];
+                        z0 = zb & 0x0Fu;
+                        z8 = zb >> 4;
+                    } else {
+                        sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
+                        const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
+                        z0 = zp & 0xFFu;
+                        z8 = zp >> 8;
+                    }
+                    const float nz0 = -(128.0f + static_cast<float>(z0));
+                    const float nz8 = -(128.0f + static_cast<float>(z8));
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint4 cw = *reinterpret_cast<const uint4 *>(ct + h * 512 + 16 * lane);
@@ -480,7 +493,7 @@ static bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt,
 
 q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                    void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
-                   cudaError_t *cerr)
+                   cudaError_t *cerr, bool cmp)
 {
     using namespace gm;
     *cerr = cudaSuccess;
@@ -506,14 +519,19 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
     const int grid = tiles < sm_count ? tiles : sm_count;
     const bool yf16 = (yt == Q4_F16);
     using KernFn = void (*)(CUtensorMap, Args);
-    static const KernFn kerns[8] = {
-        k_gemm<false, false, false>, k_gemm<false, true, false>, k_gemm<true, false, false>,
-        k_gemm<true, true, false>,   k_gemm<false, false, true>, k_gemm<false, true, true>,
-        k_gemm<true, false, true>,   k_gemm<true, true, true>};
-    const int variant = (narrow ? 4 : 0) + (f16 ? 2 : 0) + (yf16 ? 1 : 0);
+    static const KernFn kerns[16] = {
+        k_gemm<false, false, false, false>, k_gemm<false, true, false, false>,
+        k_gemm<true, false, false, false>,  k_gemm<true, true, false, false>,
+        k_gemm<false, false, true, false>,  k_gemm<false, true, true, false>,
+        k_gemm<true, false, true, false>,   k_gemm<true, true, true, false>,
+        k_gemm<false, false, false, true>,  k_gemm<false, true, false, true>,
+        k_gemm<true, false, false, true>,   k_gemm<true, true, false, true>,
+        k_gemm<false, false, true, true>,   k_gemm<false, true, true, true>,
+        k_gemm<true, false, true, true>,    k_gemm<true, true, true, true>};
+    const int variant = (cmp ? 8 : 0) + (narrow ? 4 : 0) + (f16 ? 2 : 0) + (yf16 ? 1 : 0);
     const KernFn kern = kerns[variant];
     const int smem = narrow ? Plan<true>::SMEM_ALLOC : Plan<false>::SMEM_ALLOC;
-    static std::atomic<bool> configured[8][64];  // concurrent first calls may both set it
+    static std::atomic<bool> configured[16][64];  // concurrent first calls may both set it
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[variant][dev].load(std::memory_order_relaxed)) {
