@@ -23,8 +23,14 @@
  *   zero    u8  [N][K/128]       canonical
  *   qw      opaque device buffer of q4_weight_bytes(N, K) bytes holding the
  *           same codes, scales and zeros in the kernels' tiled layout
- *           (written by q4_repack, read back by q4_unpack)
+ *           (written by q4_repack, read back by q4_unpack), or of
+ *           q4_weight_bytes_compact(N, K) bytes in the compact layout
+ *           (binary16 scales, 4-bit zeros; q4_repack_compact)
  *   x       [M][K] of dtype xt,  y  [M][N] of dtype yt
+ *
+ * A second quantizer, q4_quantize_sym, follows the symmetric scheme of the
+ * page "Quantization" (max|w| / 7 scales, codes stored with zero 8), into
+ * the same canonical arrays.
  *
  * Conventions shared by every entry point:
  *   - All pointers are device pointers unless stated; the caller owns all
