@@ -187,12 +187,9 @@ class Decode70B:
         synth.dev_normal_bf16(self.x.data_ptr(), xo, seed + 7777, 0, 1.0)
         self.x = self.x.view(torch.bfloat16)
         self.y = torch.empty(yo, dtype=torch.bfloat16, device=dev)
-        # one workspace per output size N: calls with the same N may share one
-        # (their counter blocks coincide); different N may not
-        self.ws = {}
-        for N in sorted({N for _, N, _ in LAYER_SHAPES}):
-            wsb = max(q4.gemv_workspace_bytes(M, N2, K) for _, N2, K in LAYER_SHAPES if N2 == N)
-            self.ws[N] = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+        # one workspace for every call: each completed call leaves it zero
+        wsb = max(q4.gemv_workspace_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
+        self.ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
         self.bytes_per_step = layers * sum(algo_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
         self.weights_bytes = layers * sum(q4.weight_bytes(N, K) for _, N, K in LAYER_SHAPES)
         self.launches_per_step = layers * len(LAYER_SHAPES)
@@ -208,7 +205,7 @@ class Decode70B:
 
     def gemv(self, l: int, i: int, path=0):
         x, y = self.views()[l][i]
-        self.q4.gemv(x, self.qw[l][i], out=y, ws=self.ws[LAYER_SHAPES[i][1]], path=path)
+        self.q4.gemv(x, self.qw[l][i], out=y, ws=self.ws, path=path)
 
     def step(self, path=0):
         for l in range(self.L):
@@ -369,6 +366,7 @@ def main():
                     help="NxK: time one GEMV shape alone (small-case mode for profilers)")
     ap.add_argument("--reps", type=int, default=3, help="launches in --case mode")
     ap.add_argument("--gemm-case", default=None, help="MxNxK: time one q4_gemm shape alone")
+    ap.add_argument("--compact", action="store_true", help="--gemm-case on compact tiles")
     ap.add_argument("--quantize-case", default=None, help="NxK: time q4_quantize on one shape")
     args = ap.parse_args()
     if args.case:
@@ -469,13 +467,15 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": f"llama70b-shaped decode step: {args.layers} layers x "
                                    f"(qkv 10240x8192, o 8192x8192, gate+up 57344x8192, "
                                    f"down 8192x28672), M={args.M}",
                        "M": args.M, "weights": "int4 asym group-128, f32 scale, u8 zero",
                        "activations": "bf16", "outputs": "bf16", "accumulate": "f32",
+                       "arithmetic": "int4 codes x bf16 activations on the tensor cores "
+                                     "(mma.sync m16n8k16, bf16 operands), f32 accumulation",
                        "weight_bytes_per_step": work.weights_bytes,
                        "algorithmic_bytes_per_step": work.bytes_per_step,
                        "us_per_token": round(t_step * 1e6, 2),
@@ -544,10 +544,11 @@ def extra_rows(q4, torch, work, pk) -> dict:
         x = x.view(torch.bfloat16).view(M, K)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         wsp = torch.zeros(max(q4.gemv_workspace_bytes(16, N, K), 256), dtype=torch.uint8, device=dev)
+        wsg = torch.zeros(max(q4.gemm_workspace_bytes(M, N, K), 256), dtype=torch.uint8, device=dev)
 
         def run_gemm():
             for l in range(L):
-                q4.gemm(x, qws[l], out=y)
+                q4.gemm(x, qws[l], out=y, ws=wsg)
 
         def run_two():
             for l in range(L):
@@ -619,19 +620,19 @@ def extra_rows(q4, torch, work, pk) -> dict:
     # the decode step at M = 8 on the same weights (80 layers, one graph)
     M = 8
     import synth
-    xs, ys, ws8 = [], [], {}
+    xs, ys = [], []
     for _, N, K in LAYER_SHAPES:
         xb = torch.empty(M * K, dtype=torch.int16, device=dev)
         synth.dev_normal_bf16(xb.data_ptr(), M * K, 808 + K, 0, 1.0)
         xs.append(xb.view(torch.bfloat16).view(M, K))
         ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
-        need = max(q4.gemv_workspace_bytes(M, N2, K2) for _, N2, K2 in LAYER_SHAPES if N2 == N)
-        ws8.setdefault(N, torch.zeros(max(need, 256), dtype=torch.uint8, device=dev))
+    ws8 = torch.zeros(max(256, max(q4.gemv_workspace_bytes(M, N, K) for _, N, K in LAYER_SHAPES)),
+                      dtype=torch.uint8, device=dev)
 
     def step8():
         for l in range(L):
             for i, (_, N, K) in enumerate(LAYER_SHAPES):
-                q4.gemv(xs[i], work.qw[l][i], out=ys[i], ws=ws8[N])
+                q4.gemv(xs[i], work.qw[l][i], out=ys[i], ws=ws8)
     g = graph_of(torch, step8)
     t = time_graph(torch, g, reps=3)
     b = L * sum(algo_bytes(M, N, K) for _, N, K in LAYER_SHAPES)
@@ -663,14 +664,13 @@ def extra_rows(q4, torch, work, pk) -> dict:
             synth.dev_normal_bf16(xb.data_ptr(), K, 707 + K, 0, 1.0)
             x7[K] = xb.view(torch.bfloat16).view(1, K)
     y7 = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for _, N, _ in shapes7]
-    ws7 = {N: torch.zeros(max(256, max(q4.gemv_workspace_bytes(1, N2, K2) for _, N2, K2 in shapes7
-                                       if N2 == N)), dtype=torch.uint8, device=dev)
-           for _, N, _ in shapes7}
+    ws7 = torch.zeros(max(256, max(q4.gemv_workspace_bytes(1, N, K) for _, N, K in shapes7)),
+                      dtype=torch.uint8, device=dev)
 
     def layer7():
         for l in range(L7):
             for i, (_, N, K) in enumerate(shapes7):
-                q4.gemv(x7[K], q7[l][i], out=y7[i], ws=ws7[N])
+                q4.gemv(x7[K], q7[l][i], out=y7[i], ws=ws7)
     g = graph_of(torch, layer7)
     t = time_graph(torch, g, reps=10) / L7
     b = sum(algo_bytes(1, N, K) for _, N, K in shapes7)
@@ -712,16 +712,25 @@ def extra_rows(q4, torch, work, pk) -> dict:
     xg = xg.view(torch.bfloat16).view(Mg, Kg)
     yg = torch.empty((Mg, Ng), dtype=torch.bfloat16, device=dev)
 
-    def grun():
-        q4.gemm(xg, qg, out=yg)
-    g = graph_of(torch, grun)
-    t = time_graph(torch, g, reps=10)
+    wsg = torch.zeros(max(256, q4.gemm_workspace_bytes(Mg, Ng, Kg)), dtype=torch.uint8, device=dev)
     flops = 2.0 * Mg * Ng * Kg
-    rows["gemm_prefill"] = {"shape": f"M={Mg} N={Ng} K={Kg} bf16", "ms": round(t * 1e3, 3),
-                            "TFLOP/s": round(flops / t / 1e12, 1),
-                            "frac_of_bf16_peak": round(flops / t / 1e12 / pk["bf16_tflops"], 4),
-                            "peak": pk["bf16_tflops"], "peak_kind": "burst, of measured"}
-    del g, xg, yg
+    for rname, qq in (("gemm_prefill", qg), ("gemm_prefill_compact", None)):
+        if qq is None:  # the same weights in compact tiles (binary16 scales, 4-bit zeros)
+            wf = torch.empty((Ng, Kg), dtype=torch.float32, device=dev)
+            synth.dev_normal_f32(wf.data_ptr(), Ng * Kg, 1000 + 2, 0, SIGMA)
+            qq = q4.QWeight.from_float(wf, compact=True)
+            del wf
+
+        def grun(qq=qq):
+            q4.gemm(xg, qq, out=yg, ws=wsg)
+        g = graph_of(torch, grun)
+        t = time_graph(torch, g, reps=10)
+        rows[rname] = {"shape": f"M={Mg} N={Ng} K={Kg} bf16", "ms": round(t * 1e3, 3),
+                       "TFLOP/s": round(flops / t / 1e12, 1),
+                       "frac_of_bf16_peak": round(flops / t / 1e12 / pk["bf16_tflops"], 4),
+                       "peak": pk["bf16_tflops"], "peak_kind": "burst, of measured"}
+        del g
+    del xg, yg, wsg
     torch.cuda.empty_cache()
 
     # quantizers (asymmetric, symmetric): HBM-bound, 4 B read + 0.539 B
@@ -837,18 +846,19 @@ def gemm_case(args) -> int:
     dev = torch.device("cuda")
     w = torch.empty((N, K), dtype=torch.float32, device=dev)
     synth.dev_normal_f32(w.data_ptr(), N * K, 600, 0, SIGMA)
-    qw = q4.QWeight.from_float(w)
+    qw = q4.QWeight.from_float(w, compact=args.compact)
     del w
     x = torch.empty(M * K, dtype=torch.int16, device=dev)
     synth.dev_normal_bf16(x.data_ptr(), M * K, 601, 0, 1.0)
     x = x.view(torch.bfloat16).view(M, K)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    q4.gemm(x, qw, out=y)
+    ws = q4.gemm_workspace(M, N, K)
+    q4.gemm(x, qw, out=y, ws=ws)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(args.reps):
-        q4.gemm(x, qw, out=y)
+        q4.gemm(x, qw, out=y, ws=ws)
     b.record()
     b.synchronize()
     assert q4.check() == q4.OK

@@ -21,11 +21,11 @@
  *                                even k in the low nibble (page, "Code")
  *   scale   f32 [N][K/128]       canonical
  *   zero    u8  [N][K/128]       canonical
- *   qw      opaque device buffer of q4_weight_bytes(N, K) bytes holding the
- *           same codes, scales and zeros in the kernels' tiled layout
- *           (written by q4_repack, read back by q4_unpack), or of
- *           q4_weight_bytes_compact(N, K) bytes in the compact layout
- *           (binary16 scales, 4-bit zeros; q4_repack_compact)
+ *   qw      opaque device buffer of q4_weight_bytes(N, K, layout) bytes
+ *           holding the same codes, scales and zeros in one of the kernels'
+ *           tiled layouts: Q4_LAYOUT_TILED (f32 scales, u8 zeros; written by
+ *           q4_repack, read back by q4_unpack) or Q4_LAYOUT_COMPACT (binary16
+ *           scales, 4-bit zeros; q4_repack_compact)
  *   x       [M][K] of dtype xt,  y  [M][N] of dtype yt
  *
  * A second quantizer, q4_quantize_sym, follows the symmetric scheme of the
@@ -39,7 +39,8 @@
  *     default stream).
  *   - Argument errors are detected on the host before anything is launched,
  *     and nothing is written: Q4_ERR_INVALID_ARG (bad sizes, NULL pointers,
- *     K % 128 != 0, short workspace), Q4_ERR_UNSUPPORTED (M or dtype outside
+ *     K % 128 != 0, a weight buffer whose size does not match its layout,
+ *     short workspace), Q4_ERR_UNSUPPORTED (M or dtype outside
  *     what the entry point handles), Q4_ERR_MISALIGNED (a pointer without the
  *     alignment stated for it).
  *   - A failed launch returns Q4_ERR_CUDA (the CUDA error text is kept for
@@ -69,6 +70,17 @@ typedef enum {
 } q4_status;
 
 typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
+
+/* How a weight buffer `qw` holds its codes, scales and zeros (the two tiled
+ * layouts written by q4_repack and q4_repack_compact below).  The products
+ * take the layout and the buffer's byte count with every call and reject a
+ * buffer whose size does not match that layout for (N, K): a compact buffer
+ * handed over as TILED, or one written for another shape, is refused before
+ * any launch instead of being read past its end (page "Weight quantization",
+ * section "Pitfalls": converting without repacking gives garbage that still
+ * runs; page "LLM Quantization Architecture in Depth", section "Kernels and
+ * memory layout": the format is a contract). */
+typedef enum { Q4_LAYOUT_TILED = 1, Q4_LAYOUT_COMPACT = 2 } q4_layout;
 
 #define Q4_GROUP 128
 #define Q4_TILE_ROWS 16
@@ -101,9 +113,10 @@ q4_status q4_quantize(const float *w, int64_t N, int64_t K, uint8_t *packed, flo
 q4_status q4_quantize_sym(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
                           uint8_t *zero, q4_stream_t stream);
 
-/* Bytes of the tiled kernel layout for an N x K matrix: ceil(N/16) row tiles
- * times K/128 groups times Q4_TILE_BYTES.  0 for invalid sizes. */
-size_t q4_weight_bytes(int64_t N, int64_t K);
+/* Bytes of a weight buffer for an N x K matrix in `layout`: ceil(N/16) row
+ * tiles times K/128 groups times Q4_TILE_BYTES (TILED) or Q4_CMP_TILE_BYTES
+ * (COMPACT).  0 for invalid sizes or an unknown layout. */
+size_t q4_weight_bytes(int64_t N, int64_t K, q4_layout layout);
 
 /*
  * Canonical -> tiled kernel layout ("packed formats with scale interleaving",
@@ -111,7 +124,8 @@ size_t q4_weight_bytes(int64_t N, int64_t K);
  * of page "Weight quantization", section "Code", closing remark).  A
  * bijection: q4_unpack inverts it exactly.  Rows N..16*ceil(N/16)-1 of the
  * last tile are written as zeros.  qw must be 16-byte aligned and hold
- * q4_weight_bytes(N, K) bytes; it may not overlap the inputs.
+ * q4_weight_bytes(N, K, Q4_LAYOUT_TILED) bytes; it may not overlap the
+ * inputs.
  * Tile (row tile rt, group g) starts at byte (rt*(K/128) + g) * 1104:
  *   bytes [0, 1024): 32 lanes x 2 chunks of 16 B; chunk c of lane l = 4 words,
  *     word i covers k-step j = 4c+i (k = 128g + 16j .. +15) for tile rows
@@ -141,28 +155,17 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
  * byte per pair, z[i] | z[i+8] << 4; [1064, 1072) zero padding (every tile
  * stays 16-byte aligned).  4.1875 bits per weight in memory.
  *
- * q4_weight_bytes_compact: ceil(N/16) * (K/128) * 1072, 0 for invalid sizes.
+ * The buffer holds q4_weight_bytes(N, K, Q4_LAYOUT_COMPACT) bytes, and the
+ * products read it when called with Q4_LAYOUT_COMPACT.
  * q4_repack_compact: canonical -> compact tiles; arguments, alignment and
  *   errors as q4_repack.
  * q4_unpack_compact: compact tiles -> codes [N][K/2], binary16 scale bits
  *   scale16 [N][K/128], zeros [N][K/128] (one byte per group).
- * q4_gemv_compact: q4_gemv on compact tiles (tensor-core path; same
- *   arguments, workspace and errors; q4_gemv_workspace_bytes covers it).
- * q4_gemm_compact: q4_gemm on compact tiles (same arguments and errors).
- * The layout of qw is not recorded in the buffer: compact tiles go to the
- * _compact entry points only (q4_gemv, q4_gemv_path and q4_gemm read
- * 1104-byte tiles and would read past the end of a compact buffer).
  */
-size_t q4_weight_bytes_compact(int64_t N, int64_t K);
 q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uint8_t *zero,
                             int64_t N, int64_t K, void *qw, q4_stream_t stream);
 q4_status q4_unpack_compact(const void *qw, int64_t N, int64_t K, uint8_t *packed,
                             uint16_t *scale16, uint8_t *zero, q4_stream_t stream);
-q4_status q4_gemv_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                          const void *qw, void *y, q4_dtype yt, void *workspace,
-                          size_t workspace_bytes, q4_stream_t stream);
-q4_status q4_gemm_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream);
 
 /*
  * Activation group sums, xsum[m][g] = sum_{k in group g} x[m][k] accumulated
@@ -173,15 +176,18 @@ q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
                   q4_stream_t stream);
 
 /* Workspace bytes q4_gemv needs for this problem on the current device (0
- * when no split over K is used).  Layout: split-K arrival counters (one u32
- * per 32 output rows, padded to 256 B) followed by f32 partial sums.  The
- * counter block must be zero before the first call (zero-fill the buffer
- * once after allocation); every completed call leaves it zero again.  One
- * workspace may serve successive calls with the same N (their counter
- * blocks coincide, whatever M and K); a call with another N would find the
- * previous call's partial sums where its counters belong, so give each N its
- * own workspace (or zero it between them).  Calls that may run concurrently
- * need separate workspaces. */
+ * when no split over K is used), whatever the activation type, path or
+ * layout.  Layout: split-K arrival counters (one u32 per 32 output rows,
+ * padded to 256 B) followed by f32 partial sums.
+ *
+ * Workspace rule (q4_gemv, q4_gemm): zero-fill a workspace once after
+ * allocating it.  Every call that completes leaves the bytes it used zero
+ * again (the CTA that finishes a split row block clears the counter and the
+ * partial sums it consumed), so one workspace of the largest size needed
+ * may serve any sequence of calls on one stream -- any shape, type or
+ * layout, GEMV and GEMM alike.  Calls that may run at the same time on the
+ * GPU (other streams) need separate workspaces.  After a call whose bounded
+ * wait ran out (q4_check returns Q4_ERR_TIMEOUT) zero it again. */
 size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -189,15 +195,26 @@ size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   scale[n][g] * (sum_{k in g} q[n][k] * x[m][k] - zero[n][g] * sum_{k in g} x[m][k])
  * (page "Weight quantization", "How it works", factored group dot; function
  * `dot`), fp32 accumulation, dequantization fused in registers.
- * x: [M][K] (xt = F32, BF16 or F16), qw: tiled layout from q4_repack, y:
- * [M][N] (yt = F32, BF16 or F16, rounded to nearest even from f32).
+ * x: [M][K] (xt = F32, BF16 or F16); qw: a weight buffer in `layout`
+ * (q4_repack: Q4_LAYOUT_TILED; q4_repack_compact: Q4_LAYOUT_COMPACT) of
+ * qw_bytes bytes, which must equal q4_weight_bytes(N, K, layout); y: [M][N]
+ * (yt = F32, BF16 or F16, rounded to nearest even from f32).
  * x, qw, y and workspace must be 16-byte aligned; workspace may be NULL when
  * q4_gemv_workspace_bytes returns 0.  Errors: UNSUPPORTED for M outside
- * [1, 16]; INVALID_ARG for bad sizes or a short workspace.
+ * [1, 16]; INVALID_ARG for bad sizes, an unknown layout, a qw_bytes that
+ * does not match the layout and shape, or a short workspace.
+ * Weights are read as constants: the kernel starts copying qw before it
+ * waits for the previous kernel on the stream to finish (programmatic
+ * dependent launch).  That is safe after any stream work that does not
+ * trigger dependent launches early -- copies, memsets, ordinary kernels,
+ * and every kernel of this library that writes a weight buffer -- but qw
+ * must not be written by a kernel that calls
+ * cudaTriggerProgrammaticLaunchCompletion (griddepcontrol.launch_dependents)
+ * before its writes are done.
  */
 q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                  void *y, q4_dtype yt, void *workspace, size_t workspace_bytes,
-                  q4_stream_t stream);
+                  q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt, void *workspace,
+                  size_t workspace_bytes, q4_stream_t stream);
 
 /* Kernel choice for q4_gemv_path.  FMA: CUDA-core f32 FMAs on codes turned
  * into f32 in registers (M = 1 only).  MMA: m16n8k16 tensor-core MMAs with the
@@ -209,10 +226,11 @@ q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
 #define Q4_PATH_MMA 2
 
 /* q4_gemv with an explicit kernel choice (same arguments, same results within
- * the f32 accumulation tolerance).  UNSUPPORTED for FMA with M != 1. */
+ * the f32 accumulation tolerance).  UNSUPPORTED for FMA with M != 1 or with
+ * compact tiles. */
 q4_status q4_gemv_path(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                       const void *qw, void *y, q4_dtype yt, void *workspace,
-                       size_t workspace_bytes, int path, q4_stream_t stream);
+                       const void *qw, q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt,
+                       void *workspace, size_t workspace_bytes, int path, q4_stream_t stream);
 
 /* Diagnostic for the bounded-wait machinery: launches the q4_gemv kernel for
  * this problem with its copy engine told to issue nothing, so every consumer
@@ -220,26 +238,51 @@ q4_status q4_gemv_path(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t
  * device error word; a following q4_check(stream) returns Q4_ERR_TIMEOUT.
  * No GPU fault is involved and the context stays usable. */
 q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                                   const void *qw, void *y, q4_dtype yt, void *workspace,
-                                   size_t workspace_bytes, q4_stream_t stream);
+                                   const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                                   q4_dtype yt, void *workspace, size_t workspace_bytes,
+                                   q4_stream_t stream);
 
 /*
  * Large-M W4A16 GEMM, Y[M][N] = X[M][K] * W_hat[N][K]^T (prefill; page
  * "LLM Quantization Architecture in Depth", section "Kernels and memory
- * layout": dequantize in shared memory and feed the tensor cores in the same
- * pass).  W_hat is formed tile by tile in shared memory as bf16 (or f16 for
- * f16 activations) and multiplied on the tcgen05 tensor cores with f32
- * accumulators in tensor memory.  x: [M][K] BF16 or F16; y: [M][N] BF16 or
- * F16 (f32 is UNSUPPORTED here).  Requires M >= 1, N % 16 == 0; x, qw and y
- * 16-byte aligned.  Any M: each CTA tile covers 128 weight rows and the
- * smallest of 16, 32, 64, 128 or 256 tokens that covers M (256 beyond), so
- * a batch of a few dozen tokens costs a narrow MMA, not a 256-token one.  Each w_hat is rounded once to the activation type, so the
- * product differs from the exact dequantized product by at most one rounding
- * of each w_hat (2^-9 relative for bf16) -- statistically far below
- * 1e-3 * sum|w_hat x| for non-adversarial data.
+ * layout": the kernel loads packed codes and scales, dequantizes on chip and
+ * feeds the tensor cores in the same pass).  Computed group by group as the
+ * page "Weight quantization" factors it ("How it works": one multiply per
+ * group): the tcgen05 tensor cores form D_g[n][m] = sum_{k in g} (q - zero)
+ * * x[m][k] from the exact small integers q - zero (in the activations'
+ * 16-bit type) with f32 accumulation in tensor memory, and each group's D_g
+ * is scaled by scale[n][g] and added up in f32.  No weight is rounded to
+ * 16 bits, so the result differs from the exact product only by f32
+ * rounding.
+ * x: [M][K] BF16 or F16 (16-byte aligned); qw: as for q4_gemv; y: [M][N]
+ * BF16, F16 or F32.  Any M >= 1 and N >= 1.  Each CTA tile covers 128
+ * weight rows and the smallest of 16, 32, 64 or 128 tokens that covers M
+ * (128 beyond); when the tiles are too few to fill the GPU, the groups of a
+ * tile are split over several CTAs and their f32 partial sums added in a
+ * fixed order through the workspace (q4_gemm_workspace_bytes; the
+ * workspace rule of q4_gemv_workspace_bytes applies).  Errors as q4_gemv
+ * (UNSUPPORTED for F32 activations).
  */
 q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                  void *y, q4_dtype yt, q4_stream_t stream);
+                  q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt, void *workspace,
+                  size_t workspace_bytes, q4_stream_t stream);
+
+/* Workspace bytes q4_gemm needs for this problem on the current device (0
+ * when every tile is computed by one CTA): one u32 arrival counter per
+ * tile, padded to 256 B, then f32 partial sums.  Same rule as
+ * q4_gemv_workspace_bytes. */
+size_t q4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Diagnostic for the GEMM's bounded waits: launches q4_gemm's kernel with
+ * its weight copies switched off, so the dequantizing warps' waits run out
+ * after 20 ms; every role then stops, the CTA waits for the copies and
+ * tensor-core operations it has in flight, frees its tensor memory and
+ * returns without writing y.  A following q4_check(stream) returns
+ * Q4_ERR_TIMEOUT; no GPU fault is involved and the context stays usable. */
+q4_status q4_gemm_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                                   const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                                   q4_dtype yt, void *workspace, size_t workspace_bytes,
+                                   q4_stream_t stream);
 
 /* Size of the static scratch array used by q4_gemv_noalloc (16 MiB; held on
  * every GPU that loads this library until the process exits). */
@@ -251,16 +294,19 @@ q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, c
  * passes only inputs and outputs; a decode loop that must never call an
  * allocator; a process whose GPU memory is reserved by another allocator).
  * No counterpart on the pages: it exists only for those callers.
- * Same arguments and results as q4_gemv (same kernels).  The workspace comes
- * from a static device array of Q4_NOALLOC_SCRATCH_BYTES; problems that need
- * more return Q4_ERR_UNSUPPORTED before any launch.  Allocates nothing.  The
- * first call on each device looks up the array's address with that device
- * current (make it before any stream capture).  All calls on a device share
- * the array and each clears its counter block with an asynchronous memset on
- * `stream`; calls that overlap on the GPU race, so order them.
+ * Same arguments and results as q4_gemv (same kernels), without the
+ * workspace.  The workspace comes from a static device array of
+ * Q4_NOALLOC_SCRATCH_BYTES; problems that need more return
+ * Q4_ERR_UNSUPPORTED before any launch.  Allocates nothing.  The first call
+ * on each device looks up the array's address with that device current
+ * (make it before any stream capture).  All calls on a device share the
+ * array and each clears the counter block it uses with an asynchronous
+ * memset on `stream` (so a call after one that timed out starts clean);
+ * calls that overlap on the GPU race, so order them.
  */
 q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream);
+                          const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                          q4_dtype yt, q4_stream_t stream);
 
 /* Synchronises `stream` and reports errors raised on the device since the
  * last check: Q4_ERR_TIMEOUT when a bounded wait inside a kernel gave up

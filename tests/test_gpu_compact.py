@@ -82,26 +82,47 @@ def test_gemv_compact_many_steps_per_cta():
 
 
 @pytest.mark.parametrize("M,N,K,xdt", [(300, 384, 1024, torch.bfloat16), (17, 160, 2048, torch.float16),
-                                       (64, 256, 384, torch.bfloat16)])
+                                       (64, 256, 384, torch.bfloat16), (5, 1000, 128, torch.bfloat16)])
 def test_gemm_compact_parity(M, N, K, xdt):
     import weight_only_int4_group_gb300 as q4
     W = synth.normal_rows(M + N, K, 0, N, 0.02)
     x, xf = x_for(xdt, M, K, seed=M + 5)
     qw = q4.QWeight.from_float(dev_f32(W), compact=True)
-    y = q4.gemm(x, qw, out_dtype=torch.bfloat16)
-    torch.cuda.synchronize()
-    assert q4.check() == q4.OK
     p, _, z, se = _oracle_compact(W)
     yr, ar = oracle.load().dot_naive(xf, p, se, z, N, K, threads=8)
-    compare(y, yr, ar, where=f"compact gemm {M}x{N}x{K}")
+    for ydt in (torch.bfloat16, torch.float32):
+        y = q4.gemm(x, qw, out_dtype=ydt)
+        torch.cuda.synchronize()
+        assert q4.check() == q4.OK
+        compare(y, yr, ar, where=f"compact gemm {M}x{N}x{K} y={ydt}")
 
 
 def test_compact_rejected_by_the_cuda_core_path():
     import weight_only_int4_group_gb300 as q4
     qw = q4.QWeight.from_float(dev_f32(np.zeros((32, 128), np.float32)), compact=True)
     x = torch.zeros((1, 128), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError):
+    with pytest.raises(q4.Q4Error) as ei:
         q4.gemv(x, qw, path=q4.PATH_FMA)
+    assert ei.value.status == q4.ERR_UNSUPPORTED
+
+
+def test_layout_mismatch_refused_and_nothing_written():
+    """Compact tiles handed over as tiled ones (and the reverse) are refused
+    before any launch; the output stays untouched."""
+    import weight_only_int4_group_gb300 as q4
+    N, K = 200, 1024
+    W = synth.normal_rows(12, K, 0, N, 0.02)
+    cq = q4.QWeight.from_float(dev_f32(W), compact=True)
+    tq = q4.QWeight.from_float(dev_f32(W))
+    x = torch.zeros((2, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((2, N), 5.0, device="cuda")
+    for bad in (q4.QWeight(cq.data, N, K, compact=False), q4.QWeight(tq.data, N, K, compact=True)):
+        for f in (q4.gemv, q4.gemm):
+            with pytest.raises(q4.Q4Error) as ei:
+                f(x, bad, out=y)
+            assert ei.value.status == q4.ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((y == 5.0).all())
 
 
 def test_gemv_compact_fullsize_sampled():

@@ -28,7 +28,7 @@ def _device_weights(N, K, seed, cols=None):
     return w
 
 
-def _check_sampled(N, K, M, seed, cols=None, nsample=24):
+def _check_sampled(N, K, M, seed, cols=None, nsample=24, product="gemv"):
     import weight_only_int4_group_gb300 as q4
     w = _device_weights(N, K, seed, cols)
     packed, scale, zero = q4.quantize(w)
@@ -36,7 +36,7 @@ def _check_sampled(N, K, M, seed, cols=None, nsample=24):
     qw = q4.QWeight(q4.repack(packed, scale, zero, N, K), N, K)
     xbits = synth.normal_bf16(seed + 1, 0, M * K).reshape(M, K)
     x = dev_bf16_bits(xbits)
-    y = q4.gemv(x, qw, out_dtype=torch.bfloat16)
+    y = (q4.gemv if product == "gemv" else q4.gemm)(x, qw, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert q4.check() == q4.OK
 
@@ -55,14 +55,21 @@ def _check_sampled(N, K, M, seed, cols=None, nsample=24):
         compare(y[:, r:r + 1], yr, ar, where=f"{N}x{K} M={M} row {r}")
 
 
-@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_70b_mlp_up(M):
     _check_sampled(28672, 8192, M, seed=101)
 
 
-@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_70b_mlp_down(M):
     _check_sampled(8192, 28672, M, seed=102)
+
+
+@pytest.mark.parametrize("N,K", [(28672, 8192), (8192, 28672)])
+def test_70b_mlp_m32_gemm(N, K):
+    """The batch sweep's M = 32 point, which goes through q4_gemm (few
+    tiles: the groups are split over the CTAs)."""
+    _check_sampled(N, K, 32, seed=103 + K, product="gemm")
 
 
 def test_70b_fused_gate_up():

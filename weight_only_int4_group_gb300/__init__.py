@@ -6,9 +6,11 @@ this package fails loudly when libq4.so has not been built; there is no
 fallback of any kind.
 
 Names follow include/q4.h: quantize, quantize_sym, repack, unpack, xsum,
-gemv, gemm, check, weight_bytes, gemv_workspace_bytes, and the compact
-layout's weight_bytes_compact, repack_compact, unpack_compact (gemv on a
-compact QWeight calls q4_gemv_compact).
+gemv, gemm, check, weight_bytes, gemv_workspace_bytes, gemm_workspace_bytes,
+repack_compact, unpack_compact, gemv_noalloc and the two timeout
+self-tests.  A QWeight carries its layout (TILED or COMPACT), and every
+product call passes that layout and the buffer's byte count to the library,
+which refuses a mismatch.
 """
 from __future__ import annotations
 
@@ -28,6 +30,7 @@ GEMV_MAX_M = 16
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
 F32, BF16, F16 = 0, 1, 2
+LAYOUT_TILED, LAYOUT_COMPACT = 1, 2
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 
 _DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
@@ -50,30 +53,31 @@ def _load():
     P, I, Z, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
     lib.q4_quantize.argtypes = [P, I, I, P, P, P, P]
     lib.q4_quantize_sym.argtypes = [P, I, I, P, P, P, P]
-    lib.q4_weight_bytes.argtypes = [I, I]
+    lib.q4_weight_bytes.argtypes = [I, I, S]
     lib.q4_weight_bytes.restype = Z
     lib.q4_repack.argtypes = [P, P, P, I, I, P, P]
     lib.q4_unpack.argtypes = [P, I, I, P, P, P, P]
-    lib.q4_weight_bytes_compact.argtypes = [I, I]
-    lib.q4_weight_bytes_compact.restype = Z
     lib.q4_repack_compact.argtypes = [P, P, P, I, I, P, P]
     lib.q4_unpack_compact.argtypes = [P, I, I, P, P, P, P]
-    lib.q4_gemv_compact.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
-    lib.q4_gemm_compact.argtypes = [P, S, I, I, I, P, P, S, P]
     lib.q4_xsum.argtypes = [P, S, I, I, P, P]
     lib.q4_gemv_workspace_bytes.argtypes = [I, I, I]
     lib.q4_gemv_workspace_bytes.restype = Z
-    lib.q4_gemv.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
-    lib.q4_gemv_path.argtypes = [P, S, I, I, I, P, P, S, P, Z, S, P]
-    lib.q4_gemv_timeout_selftest.argtypes = [P, S, I, I, I, P, P, S, P, Z, P]
-    lib.q4_gemm.argtypes = [P, S, I, I, I, P, P, S, P]
+    lib.q4_gemm_workspace_bytes.argtypes = [I, I, I]
+    lib.q4_gemm_workspace_bytes.restype = Z
+    prod = [P, S, I, I, I, P, S, Z, P, S, P, Z, P]  # x, xt, M, N, K, qw, layout, bytes, y, yt, ws, wsb, stream
+    lib.q4_gemv.argtypes = prod
+    lib.q4_gemv_path.argtypes = prod[:-1] + [S, P]
+    lib.q4_gemv_timeout_selftest.argtypes = prod
+    lib.q4_gemm.argtypes = prod
+    lib.q4_gemm_timeout_selftest.argtypes = prod
+    lib.q4_gemv_noalloc.argtypes = [P, S, I, I, I, P, S, Z, P, S, P]
     lib.q4_check.argtypes = [P]
     lib.q4_status_str.argtypes = [S]
     lib.q4_status_str.restype = ctypes.c_char_p
     lib.q4_last_cuda_error.restype = ctypes.c_char_p
     for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_repack_compact",
-              "q4_unpack_compact", "q4_gemv_compact", "q4_gemm_compact", "q4_xsum", "q4_gemv", "q4_gemv_path",
-              "q4_gemv_timeout_selftest", "q4_gemm", "q4_check"):
+              "q4_unpack_compact", "q4_xsum", "q4_gemv", "q4_gemv_path", "q4_gemv_timeout_selftest",
+              "q4_gemm", "q4_gemm_timeout_selftest", "q4_gemv_noalloc", "q4_check"):
         getattr(lib, f).restype = S
     return lib
 
@@ -105,16 +109,20 @@ def _cuda(t: torch.Tensor, name: str):
 
 
 # ------------------------------------------------------------------ API
-def weight_bytes(N: int, K: int) -> int:
-    return int(_lib.q4_weight_bytes(N, K))
+def weight_bytes(N: int, K: int, layout: int = LAYOUT_TILED) -> int:
+    return int(_lib.q4_weight_bytes(N, K, layout))
 
 
 def weight_bytes_compact(N: int, K: int) -> int:
-    return int(_lib.q4_weight_bytes_compact(N, K))
+    return weight_bytes(N, K, LAYOUT_COMPACT)
 
 
 def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(_lib.q4_gemv_workspace_bytes(M, N, K))
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.q4_gemm_workspace_bytes(M, N, K))
 
 
 def quantize(w: torch.Tensor, stream=None, symmetric: bool = False):
@@ -170,7 +178,7 @@ def repack_compact(packed: torch.Tensor, scale: torch.Tensor, zero: torch.Tensor
     """Canonical arrays -> compact tiles (binary16 scales, 4-bit zeros)."""
     for t, n in ((packed, "packed"), (scale, "scale"), (zero, "zero")):
         _cuda(t, n)
-    nb = weight_bytes_compact(N, K)
+    nb = weight_bytes(N, K, LAYOUT_COMPACT)
     if nb == 0:
         raise ValueError(f"invalid shape {N}x{K}")
     if out is None:
@@ -202,12 +210,20 @@ def xsum(x: torch.Tensor, stream=None) -> torch.Tensor:
 
 @dataclass
 class QWeight:
-    """A weight matrix in the tiled kernel layout (compact: binary16 scales
-    and 4-bit zeros)."""
-    data: torch.Tensor  # uint8 [weight_bytes(N, K)] or [weight_bytes_compact(N, K)]
+    """A weight matrix in one of the tiled kernel layouts (compact: binary16
+    scales and 4-bit zeros)."""
+    data: torch.Tensor  # uint8 [weight_bytes(N, K, layout)]
     N: int
     K: int
     compact: bool = False
+
+    @property
+    def layout(self) -> int:
+        return LAYOUT_COMPACT if self.compact else LAYOUT_TILED
+
+    @property
+    def nbytes(self) -> int:
+        return self.data.numel() * self.data.element_size()
 
     @classmethod
     def from_float(cls, w: torch.Tensor, stream=None, symmetric: bool = False,
@@ -219,59 +235,91 @@ class QWeight:
         return cls(repack(packed, scale, zero, N, K, stream=stream), N, K)
 
 
-def workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
-    """A zero-filled workspace for q4_gemv (None when none is needed)."""
-    nb = gemv_workspace_bytes(M, N, K)
+def _zeros(nb: int, device) -> torch.Tensor | None:
     if nb == 0:
         return None
     return torch.zeros(nb, dtype=torch.uint8, device=device or torch.cuda.current_device())
 
 
-def gemv(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
-         ws: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
-    """y [M][N] = x [M][K] * w_hat^T for 1 <= M <= 16."""
+def workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
+    """A zero-filled workspace for q4_gemv (None when none is needed)."""
+    return _zeros(gemv_workspace_bytes(M, N, K), device)
+
+
+def gemm_workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
+    """A zero-filled workspace for q4_gemm (None when none is needed)."""
+    return _zeros(gemm_workspace_bytes(M, N, K), device)
+
+
+def _ws(ws):
+    return (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
+
+
+def _product_args(x: torch.Tensor, qw: QWeight, out_dtype, out):
     _cuda(x, "x")
     M, K = x.shape
     if K != qw.K:
         raise ValueError(f"x has K={K}, weight has K={qw.K}")
     if out is None:
         out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)
+    return M, K, out
+
+
+def gemv(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
+         ws: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y [M][N] = x [M][K] * w_hat^T for 1 <= M <= 16."""
+    M, K, out = _product_args(x, qw, out_dtype, out)
     if ws is None:
         ws = workspace(M, qw.N, K, x.device)
-    wsp, wsb = (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
-    if qw.compact:
-        if path != PATH_AUTO:
-            raise ValueError("compact weights run on the default (tensor-core) path only")
-        _ok(_lib.q4_gemv_compact(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
-                                 out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, _stream(stream)),
-            "q4_gemv_compact")
-        return out
+    wsp, wsb = _ws(ws)
     _ok(_lib.q4_gemv_path(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
-                          out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, path, _stream(stream)),
-        "q4_gemv")
+                          qw.layout, qw.nbytes, out.data_ptr(), _DTYPE[out.dtype], wsp, wsb,
+                          path, _stream(stream)), "q4_gemv")
+    return out
+
+
+def gemv_noalloc(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """q4_gemv_noalloc: q4_gemv with the library's static scratch array as
+    its workspace (for callers that cannot allocate device memory)."""
+    M, K, out = _product_args(x, qw, out_dtype, out)
+    _ok(_lib.q4_gemv_noalloc(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(),
+                             qw.layout, qw.nbytes, out.data_ptr(), _DTYPE[out.dtype],
+                             _stream(stream)), "q4_gemv_noalloc")
     return out
 
 
 def gemv_timeout_selftest(x: torch.Tensor, qw: QWeight, out: torch.Tensor,
                           ws: torch.Tensor | None = None, stream=None) -> None:
     M, K = x.shape
-    wsp, wsb = (0, 0) if ws is None else (ws.data_ptr(), ws.numel())
+    wsp, wsb = _ws(ws)
     _ok(_lib.q4_gemv_timeout_selftest(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K,
-                                      qw.data.data_ptr(), out.data_ptr(), _DTYPE[out.dtype],
-                                      wsp, wsb, _stream(stream)), "q4_gemv_timeout_selftest")
+                                      qw.data.data_ptr(), qw.layout, qw.nbytes, out.data_ptr(),
+                                      _DTYPE[out.dtype], wsp, wsb, _stream(stream)),
+        "q4_gemv_timeout_selftest")
 
 
 def gemm(x: torch.Tensor, qw: QWeight, out_dtype=None, out: torch.Tensor | None = None,
-         stream=None) -> torch.Tensor:
-    """Y [M][N] = X [M][K] * w_hat^T on the tcgen05 tensor cores (large M)."""
-    _cuda(x, "x")
-    M, K = x.shape
-    if out is None:
-        out = torch.empty((M, qw.N), dtype=out_dtype or x.dtype, device=x.device)
-    fn, name = (_lib.q4_gemm_compact, "q4_gemm_compact") if qw.compact else (_lib.q4_gemm, "q4_gemm")
-    _ok(fn(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(), out.data_ptr(),
-           _DTYPE[out.dtype], _stream(stream)), name)
+         ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y [M][N] = X [M][K] * w_hat^T on the tcgen05 tensor cores (any M)."""
+    M, K, out = _product_args(x, qw, out_dtype, out)
+    if ws is None:
+        ws = gemm_workspace(M, qw.N, K, x.device)
+    wsp, wsb = _ws(ws)
+    _ok(_lib.q4_gemm(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K, qw.data.data_ptr(), qw.layout,
+                     qw.nbytes, out.data_ptr(), _DTYPE[out.dtype], wsp, wsb, _stream(stream)),
+        "q4_gemm")
     return out
+
+
+def gemm_timeout_selftest(x: torch.Tensor, qw: QWeight, out: torch.Tensor,
+                          ws: torch.Tensor | None = None, stream=None) -> None:
+    M, K = x.shape
+    wsp, wsb = _ws(ws)
+    _ok(_lib.q4_gemm_timeout_selftest(x.data_ptr(), _DTYPE[x.dtype], M, qw.N, K,
+                                      qw.data.data_ptr(), qw.layout, qw.nbytes, out.data_ptr(),
+                                      _DTYPE[out.dtype], wsp, wsb, _stream(stream)),
+        "q4_gemm_timeout_selftest")
 
 
 def check(stream=None) -> int:

@@ -1,6 +1,7 @@
 // api.cu -- the exported C ABI (include/q4.h): host-side argument checks,
 // plan selection and launches.  Nothing here allocates or synchronises except
-// q4_check.
+// q4_check.  Every product call names its weight layout and the weight
+// buffer's byte count, checked against each other before anything runs.
 #include <stdio.h>
 #include <string.h>
 
@@ -14,7 +15,7 @@ namespace q4 {
 
 static thread_local char t_last_error[256] = "";
 
-static q4_status cuda_fail(cudaError_t e)
+q4_status cuda_fail(cudaError_t e)
 {
     snprintf(t_last_error, sizeof(t_last_error), "%s: %s", cudaGetErrorName(e),
              cudaGetErrorString(e));
@@ -63,13 +64,31 @@ static inline bool sizes_ok(int64_t N, int64_t K)
            N * K <= (1LL << 40);
 }
 
+size_t weight_bytes(int64_t N, int64_t K, q4_layout layout)
+{
+    if (!sizes_ok(N, K)) return 0;
+    const size_t tile = layout == Q4_LAYOUT_TILED ? TILE_BYTES
+                        : layout == Q4_LAYOUT_COMPACT ? CMP_TILE_BYTES
+                                                      : 0;
+    return static_cast<size_t>((N + TILE_ROWS - 1) / TILE_ROWS) * static_cast<size_t>(K / G) * tile;
+}
+
+// The weight buffer matches its declared layout and shape byte for byte.
+static inline bool weights_ok(int64_t N, int64_t K, q4_layout layout, size_t qw_bytes)
+{
+    const size_t need = weight_bytes(N, K, layout);
+    return need != 0 && qw_bytes == need;
+}
+
 static q4_status gemv_common(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                             const void *qw, void *y, q4_dtype yt, void *workspace,
-                             size_t workspace_bytes, cudaStream_t stream, int path,
-                             int debug_no_copy, uint64_t wait_ns, bool cmp = false)
+                             const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                             q4_dtype yt, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, int path, int debug_no_copy, uint64_t wait_ns)
 {
     if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
     if (!sizes_ok(N, K) || N > (1LL << 28)) return Q4_ERR_INVALID_ARG;
+    if (!weights_ok(N, K, layout, qw_bytes)) return Q4_ERR_INVALID_ARG;
+    const bool cmp = layout == Q4_LAYOUT_COMPACT;
     if (M < 1 || M > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED;
     if (!valid_dtype(xt) || !valid_dtype(yt)) return Q4_ERR_UNSUPPORTED;
     if (path == PATH_FMA && (M != 1 || cmp)) return Q4_ERR_UNSUPPORTED;
@@ -131,11 +150,9 @@ q4_status q4_quantize_sym(const float *w, int64_t N, int64_t K, uint8_t *packed,
     return quantize_common(w, N, K, packed, scale, zero, true, stream);
 }
 
-size_t q4_weight_bytes(int64_t N, int64_t K)
+size_t q4_weight_bytes(int64_t N, int64_t K, q4_layout layout)
 {
-    if (!sizes_ok(N, K)) return 0;
-    return static_cast<size_t>((N + TILE_ROWS - 1) / TILE_ROWS) * static_cast<size_t>(K / G) *
-           TILE_BYTES;
+    return weight_bytes(N, K, layout);
 }
 
 q4_status q4_repack(const uint8_t *packed, const float *scale, const uint8_t *zero, int64_t N,
@@ -156,13 +173,6 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
     const cudaError_t e = unpack_launch(static_cast<const uint8_t *>(qw), N, K, packed, scale,
                                         zero, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
-}
-
-size_t q4_weight_bytes_compact(int64_t N, int64_t K)
-{
-    if (!sizes_ok(N, K)) return 0;
-    return static_cast<size_t>((N + TILE_ROWS - 1) / TILE_ROWS) * static_cast<size_t>(K / G) *
-           CMP_TILE_BYTES;
 }
 
 q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uint8_t *zero,
@@ -218,66 +228,78 @@ size_t q4_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K)
 }
 
 q4_status q4_gemv(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                  void *y, q4_dtype yt, void *workspace, size_t workspace_bytes,
-                  q4_stream_t stream)
+                  q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt, void *workspace,
+                  size_t workspace_bytes, q4_stream_t stream)
 {
-    return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
+    return gemv_common(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 0, 1000000000ull);
 }
 
-q4_status q4_gemv_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                          const void *qw, void *y, q4_dtype yt, void *workspace,
-                          size_t workspace_bytes, q4_stream_t stream)
-{
-    return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
-                       reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 0, 1000000000ull, true);
-}
-
 q4_status q4_gemv_path(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                       const void *qw, void *y, q4_dtype yt, void *workspace,
-                       size_t workspace_bytes, int path, q4_stream_t stream)
+                       const void *qw, q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt,
+                       void *workspace, size_t workspace_bytes, int path, q4_stream_t stream)
 {
     if (path != PATH_AUTO && path != PATH_FMA && path != PATH_MMA) return Q4_ERR_UNSUPPORTED;
-    return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
+    return gemv_common(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream), path, 0, 1000000000ull);
 }
 
 q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                                   const void *qw, void *y, q4_dtype yt, void *workspace,
-                                   size_t workspace_bytes, q4_stream_t stream)
+                                   const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                                   q4_dtype yt, void *workspace, size_t workspace_bytes,
+                                   q4_stream_t stream)
 {
-    return gemv_common(x, xt, M, N, K, qw, y, yt, workspace, workspace_bytes,
+    return gemv_common(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream), PATH_AUTO, 1, 20000000ull);
 }
 
 static q4_status gemm_common(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                             const void *qw, void *y, q4_dtype yt, q4_stream_t stream, bool cmp)
+                             const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                             q4_dtype yt, void *workspace, size_t workspace_bytes,
+                             q4_stream_t stream, int debug_no_copy, uint64_t wait_ns)
 {
     if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
-    if (M < 1 || M > (1LL << 30) || !sizes_ok(N, K) || N % 16 != 0 || N > (1LL << 30))
-        return Q4_ERR_INVALID_ARG;
-    if ((xt != Q4_BF16 && xt != Q4_F16) || (yt != Q4_BF16 && yt != Q4_F16))
-        return Q4_ERR_UNSUPPORTED;
-    if (!aligned16(x) || !aligned16(qw) || !aligned16(y)) return Q4_ERR_MISALIGNED;
+    if (M < 1 || M > (1LL << 30) || !sizes_ok(N, K) || N > (1LL << 30)) return Q4_ERR_INVALID_ARG;
+    if (!weights_ok(N, K, layout, qw_bytes)) return Q4_ERR_INVALID_ARG;
+    if ((xt != Q4_BF16 && xt != Q4_F16) || !valid_dtype(yt)) return Q4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(y) || !aligned16(workspace))
+        return Q4_ERR_MISALIGNED;
     const DevInfo *d = dev_info();
     if (!d) return cuda_fail(cudaGetLastError());
+    const GemmPlan plan = gemm_plan(M, N, K, d->sm_count);
+    if (plan.workspace > 0 && (!workspace || workspace_bytes < plan.workspace))
+        return Q4_ERR_INVALID_ARG;
     cudaError_t e = cudaSuccess;
-    const q4_status st = gemm_run(x, xt, M, N, K, qw, y, yt, d->sm_count, d->err,
-                                  reinterpret_cast<cudaStream_t>(stream), &e, cmp);
+    const q4_status st = gemm_run(plan, x, xt, M, N, K, static_cast<const uint8_t *>(qw),
+                                  layout == Q4_LAYOUT_COMPACT, y, yt, workspace, d->err, wait_ns,
+                                  debug_no_copy, reinterpret_cast<cudaStream_t>(stream), &e);
     if (st == Q4_ERR_CUDA) return cuda_fail(e);
     return st;
 }
 
 q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                  void *y, q4_dtype yt, q4_stream_t stream)
+                  q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt, void *workspace,
+                  size_t workspace_bytes, q4_stream_t stream)
 {
-    return gemm_common(x, xt, M, N, K, qw, y, yt, stream, false);
+    return gemm_common(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, workspace, workspace_bytes,
+                       stream, 0, 2000000000ull);
 }
 
-q4_status q4_gemm_compact(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                          const void *qw, void *y, q4_dtype yt, q4_stream_t stream)
+size_t q4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
-    return gemm_common(x, xt, M, N, K, qw, y, yt, stream, true);
+    if (M < 1 || M > (1LL << 30) || !sizes_ok(N, K) || N > (1LL << 30)) return 0;
+    const DevInfo *d = dev_info();
+    if (!d) return 0;
+    return gemm_plan(M, N, K, d->sm_count).workspace;
+}
+
+q4_status q4_gemm_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                                   const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                                   q4_dtype yt, void *workspace, size_t workspace_bytes,
+                                   q4_stream_t stream)
+{
+    return gemm_common(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, workspace, workspace_bytes,
+                       stream, 1, 20000000ull);
 }
 
 q4_status q4_check(q4_stream_t stream)

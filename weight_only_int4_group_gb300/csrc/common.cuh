@@ -36,6 +36,13 @@ constexpr int CMP_ZERO_OFF = 1056;
 constexpr unsigned int ERR_TIMEOUT = 1u;
 unsigned int *device_error_word();  // host: address on the current device
 
+// Host: keeps the CUDA error's text for q4_last_cuda_error (this thread) and
+// returns Q4_ERR_CUDA.
+q4_status cuda_fail(cudaError_t e);
+
+// Host: bytes of an N x K weight buffer in `layout` (0 if invalid).
+size_t weight_bytes(int64_t N, int64_t K, q4_layout layout);
+
 // ----------------------------------------------------------------- inline PTX
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -255,9 +262,23 @@ cudaError_t repack_compact_launch(const uint8_t *packed, const float *scale, con
                                   int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
 cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed,
                                   uint16_t *scale16, uint8_t *zero, cudaStream_t s);
-q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                   void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
-                   cudaError_t *cerr, bool cmp = false);
+// Large-M GEMM plan: tiles of 128 weight rows x bt tokens; either every
+// tile is computed by one CTA (split == false, tiles dealt round robin) or
+// the tiles' groups form one sequence of items cut into equal contiguous
+// ranges, one per CTA, with partial sums through the workspace.
+struct GemmPlan {
+    int bt;        // tokens per tile: 16, 32, 64 or 128
+    int mt, nt;    // tiles along M and along N
+    int grid;      // persistent CTAs
+    bool split;    // groups of a tile may be spread over several CTAs
+    int maxc;      // most CTAs sharing one tile (1 without split)
+    size_t workspace;
+};
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count);
+q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                   const uint8_t *qw, bool cmp, void *y, q4_dtype yt, void *workspace,
+                   unsigned int *err, uint64_t wait_ns, int debug_no_copy, cudaStream_t s,
+                   cudaError_t *cerr);
 cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
                         cudaStream_t s);
 

@@ -1,41 +1,52 @@
-// gemm_tc.cu -- large-M W4A16 GEMM on the sm_103a tcgen05 tensor cores.
+// gemm_tc.cu -- W4A16 GEMM on the sm_103a tcgen05 tensor cores, exact per group.
 //
 // Y[M][N] = X[M][K] * W_hat[N][K]^T with W_hat = (q - zero) * scale per group
-// of 128 along K (page "Weight quantization", "How it works"), the weights
-// dequantized tile by tile in shared memory and fed to the tensor cores in the
-// same pass (page "LLM Quantization Architecture in Depth", "Kernels and
-// memory layout"); the fp weights never reach HBM.
+// of 128 along K (page "Weight quantization", "How it works"), computed the
+// way that page factors the product, one multiply per group: for every group
+// g the tensor cores form
+//     D_g[n][m] = sum_{k in g} (q[n][k] - zero[n][g]) * x[m][k]
+// from the small integers q - zero (exact in bf16 or f16, the activations'
+// type) with f32 accumulation in tensor memory, and
+//     Y^T[n][m] += scale[n][g] * D_g[n][m]
+// is added up in f32 registers.  No weight is ever rounded to 16 bits, so the
+// result differs from the exact product by f32 rounding only.  The packed
+// codes are unpacked on chip and the floating-point weights never reach HBM
+// (page "LLM Quantization Architecture in Depth", "Kernels and memory
+// layout").
 //
-// One persistent CTA per SM, 15 warps with fixed roles:
-//   warp 0     activation producer: tiles of X by 2-D tensor TMA (128-byte
-//              swizzle);
-//   warp 1     allocates tensor memory; one thread issues tcgen05.mma;
-//   warps 2-9  dequantize, one 16-row tile each: codes -> bf16 (or f16)
-//              w_hat = (q - zero) * scale, written in the K-major
-//              128-byte-swizzled layout the MMA reads;
-//   warps 10-13 epilogue: tcgen05.ld of the accumulators -> bf16/f16 ->
-//              coalesced stores (32 consecutive outputs of one token per
-//              warp instruction);
-//   warp 14    weight producer: packed tiles by 1-D bulk copies, in its own
-//              ring, so the weight stream runs as far ahead as its ring
-//              allows whatever the activation ring is doing.
-// CTA tile: 128 weight rows x BT tokens, K in stages of one group (128),
-// where BT is the smallest of 16, 32, 64, 128 and 256 that covers M (256 for
-// larger M): a few tokens get a narrow MMA and a short activation box
-// instead of a 256-row one that is mostly padding.  The MMA computes the
-// transposed product Y^T = W_hat * X^T: A = the dequantized weight tile (128
-// rows), B = the BT activation rows, one 128 x BT x 16 MMA per 16 k, so each
-// weight tile is dequantized once per BT tokens.  A stage holds one group's
-// activations and its dequantized weights under one "full" barrier (the
-// activation bytes plus the eight dequantizing warps) and one "empty"
-// barrier (the MMAs that read it): a barrier wait costs the waiting thread
-// a few hundred cycles even when the phase is already complete, so the MMA
-// thread waits once and commits once per eight MMAs.  Accumulator: 128
-// lanes x BT f32 columns in tensor memory, double-buffered (buffers 256
-// columns apart) so the epilogue of one tile overlaps the MMAs of the next.
+// One persistent CTA per SM, 16 warps with fixed roles:
+//   warp 0      activation producer: X tiles by 2-D tensor TMA (128-byte
+//               swizzle, K-major), one stage per group;
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma;
+//   warp 2      weight producer: the group's 8 packed tiles (16 rows each)
+//               by 1-D bulk copies into a ring of code stages;
+//   warp 3      idle;
+//   warps 4-7   operand builders, one per tensor-memory lane quadrant: each
+//               thread owns one weight row, turns its 128 codes into 64
+//               packed (q - zero) pairs with one LOP3 and one packed FMA per
+//               pair, and stores them with tcgen05.st as the MMA's A operand
+//               (tensor memory, not shared memory: shared memory carries only
+//               the activations and the packed codes);
+//   warps 8-15  rescale and epilogue: per group each thread loads its row's
+//               D_g columns (tcgen05.ld), releases the buffer and adds
+//               scale * D_g into its f32 accumulators; at the end of a tile
+//               it stores the row (or a partial sum, below).
+// Tensor memory (512 columns): D_g double-buffered at columns 0 and 128 (128
+// weight rows x up to 128 tokens), A stages of one group at 256 + 64 s.
+// A CTA tile is 128 weight rows x BT tokens, BT the smallest of 16, 32, 64,
+// 128 that covers M (128 beyond): one 128 x BT x 16 MMA per 16 k, A from
+// tensor memory, B = the activation rows from shared memory.
+//
+// Work: when there are many tiles every CTA takes whole tiles in turn; when
+// there are few (a few dozen tokens), the tiles' groups form one sequence of
+// items cut into equal contiguous ranges, one per CTA, and a tile whose
+// groups are spread over several CTAs is finished by the last of them to
+// arrive, which adds the f32 partial sums of all contributors in CTA order
+// (results do not depend on timing) and clears them for the next call.
+//
 // Every barrier wait is bounded; on expiry the CTA raises the device error
-// word, stops, drains its copies and MMAs, frees its tensor memory and
-// returns.
+// word, every role stops, the copies and tensor-core operations in flight are
+// waited for, tensor memory is freed and the kernel returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,36 +57,29 @@
 namespace q4 {
 namespace gm {
 
-constexpr int BM = 256, SUB = 128, BN = 128, BK = 64;
-constexpr int NARROW_MAX = 64;             // token tiles up to this use the narrow plan
-constexpr int RT = BN / TILE_ROWS;         // 8 row tiles per weight tile
-constexpr int A_BOX = SUB * BK * 2;        // 16384: one 128 x 64 activation box
-constexpr int B_HALF = BN * BK * 2;        // 16384: dequantized weights of 64 k
-constexpr int C_STAGE = RT * TILE_BYTES;   // 8832: packed tiles of one group
-constexpr int THREADS = 480;
+constexpr int BN = 128;                    // weight rows per tile
+constexpr int RT = BN / TILE_ROWS;         // 8 packed tiles per group
+constexpr int C_STAGE = RT * TILE_BYTES;   // 8832 bytes of codes per group (compact: 8576 used)
+constexpr int THREADS = 512;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COL = 256;            // first tensor-memory column of the A stages
+constexpr int NS = 4;                      // activation / A stages
+constexpr int NSC = 8;                     // scale hand-off slots
+constexpr int BAND = 8;                    // token tiles per raster band
 
-// Shared-memory plan of one CTA: NS stages of one group each (activations in
-// two 64-wide swizzled halves, then the dequantized weights in two halves),
-// NC packed-code stages.  The narrow plan (token tiles of at most 64 rows)
-// needs 8 KB activation halves and keeps 4 stages; the wide plan 32 KB
-// halves and 2 stages (the same 256 k of lookahead).
-template <bool NARROW>
+template <int BT>
 struct Plan {
-    static constexpr int NS = NARROW ? 4 : 2;
-    static constexpr int NC = 3;
-    static constexpr int A_HALF = NARROW ? NARROW_MAX * BK * 2 : 2 * A_BOX;
-    static constexpr int A_ST = 2 * A_HALF;
-    static constexpr int B_ST = 2 * B_HALF;
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + NS * A_ST;
-    static constexpr int OFF_C = OFF_B + NS * B_ST;
-    static constexpr int OFF_BAR = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;
-    static constexpr int BAR_BYTES = (2 * (NS + NC) + 5) * 8 + 8;
-    static constexpr int SMEM_USED = OFF_BAR + 256;
+    static constexpr int NC = BT >= 128 ? 6 : 8;  // code stages
+    static constexpr int X_HALF = BT * 64 * 2;    // one 64-k half of a group's activations
+    static constexpr int X_ST = 2 * X_HALF;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_C = NS * X_ST;
+    static constexpr int OFF_S = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;  // scale slots
+    static constexpr int OFF_BAR = OFF_S + NSC * BN * 4;
+    static constexpr int NBAR = 3 * NS + 2 * NC + 2 * NSC + 5;
+    static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
-    static_assert(OFF_B % 1024 == 0 && OFF_C % 16 == 0, "alignment");
-    static_assert(BAR_BYTES <= 256, "barrier area");
+    static_assert(X_HALF % 1024 == 0, "swizzled halves start on 1024-byte boundaries");
     static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
 };
 
@@ -128,13 +132,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab, uint32_t n)
     return (1u << 4) | (ab << 7) | (ab << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate)
+// D (tensor memory) [+]= A (tensor memory) * B (shared memory descriptor).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -145,88 +150,178 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
+#define Q4_R8(a, o) "r"(a[o + 0]), "r"(a[o + 1]), "r"(a[o + 2]), "r"(a[o + 3]), "r"(a[o + 4]), \
+    "r"(a[o + 5]), "r"(a[o + 6]), "r"(a[o + 7])
+#define Q4_W8(a, o) "=r"(a[o + 0]), "=r"(a[o + 1]), "=r"(a[o + 2]), "=r"(a[o + 3]), \
+    "=r"(a[o + 4]), "=r"(a[o + 5]), "=r"(a[o + 6]), "=r"(a[o + 7])
+
+// 32 consecutive 32-bit columns of this warp's 32 lanes <- v (thread i: lane i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        Q4_R8(v, 0), Q4_R8(v, 8), Q4_R8(v, 16), Q4_R8(v, 24)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// v <- 32 (or 16) consecutive columns of this warp's lanes; completes at tmem_wait_ld.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : Q4_W8(v, 0), Q4_W8(v, 8), Q4_W8(v, 16), Q4_W8(v, 24)
+        : "r"(taddr)
+        : "memory");
 }
-
-// Two codes of a bf16 pair (128 + q_a | 128 + q_b) -> (q - zero) * scale,
-// rounded once from f32 to bf16/f16, packed (a in the low half).
-template <bool F16>
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t p, float neg_z, float s)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[32])
 {
-    float2 v = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
-    v = __fadd2_rn(v, make_float2(neg_z, neg_z));  // exact: small integers
-    v = __fmul2_rn(v, make_float2(s, s));
-    if (F16) {
-        const __half2 h = __float22half2_rn(v);
-        return *reinterpret_cast<const uint32_t *>(&h);
-    }
-    const __nv_bfloat162 b = __float22bfloat162_rn(v);
-    return *reinterpret_cast<const uint32_t *>(&b);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15}, [%16];"
+        : Q4_W8(v, 0), Q4_W8(v, 8)
+        : "r"(taddr)
+        : "memory");
+}
+#undef Q4_R8
+#undef Q4_W8
+
+// d = a * 1 + c on a pair of 16-bit floats (bf16 or f16); exact here: a is
+// offset + q, c = -(offset + zero), the difference a small integer.
+template <bool F16>
+__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t c)
+{
+    uint32_t d;
+    if (F16)
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3C003C00u), "r"(c));
+    else
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(c));
+    return d;
 }
 
 struct Args {
     const uint8_t *qw;
     void *y;
+    q4_dtype yt;
     int M, N, K;
-    int bt;      // tokens per tile: 16, 32, 64, 128 or 256
-    int mt, nt;  // tiles along M (bt rows) and N (128 rows)
+    int mt, nt;            // tiles along M (bt tokens) and N (128 rows)
+    int split;             // 1: contiguous item ranges, partial sums through the workspace
+    int maxc;              // most CTAs sharing one tile
+    unsigned int *count;   // [tiles] arrival counters (split)
+    float *partial;        // [tiles][maxc][128 rows][bt] partial sums (split)
     uint64_t wait_ns;
     unsigned int *err;
+    int debug_no_copy;     // the weight producer copies nothing (bounded-wait self-test)
 };
 
-// F16: activations (and the dequantized weights) are f16, else bf16.
-// YF16: outputs are f16, else bf16.  NARROW: the shared-memory plan for
-// token tiles of at most 64 rows.  CMP: compact tiles (binary16 scale
-// pairs, zero nibbles, 1072 bytes; a code stage still fits 8 of them).
-template <bool F16, bool YF16, bool NARROW, bool CMP>
+// Tile t of the raster: bands of BAND token tiles; inside a band the token
+// tile runs fastest, so the CTAs working at the same time share few weight
+// tiles and few activation tiles.
+__device__ __forceinline__ void tile_coords(int t, int mt, int nt, int &mb, int &nb)
+{
+    const int band = t / (BAND * nt);
+    const int bm = min(BAND, mt - band * BAND);
+    const int r = t - band * BAND * nt;
+    mb = band * BAND + r % bm;
+    nb = r / bm;
+}
+
+// The CTA's next unit of work: a tile and its group range [g0, g1).
+struct Cursor {
+    int64_t pos, end;
+};
+__device__ __forceinline__ bool next_unit(const Args &a, int NG, Cursor &c, int &tile, int &g0,
+                                          int &g1)
+{
+    if (c.pos >= c.end) return false;
+    if (a.split) {
+        tile = static_cast<int>(c.pos / NG);
+        g0 = static_cast<int>(c.pos % NG);
+        const int64_t left = c.end - c.pos;
+        g1 = static_cast<int>(left < NG - g0 ? g0 + left : NG);
+        c.pos += g1 - g0;
+    } else {
+        tile = static_cast<int>(c.pos);
+        g0 = 0;
+        g1 = NG;
+        c.pos += gridDim.x;
+    }
+    return true;
+}
+
+// CTA owning item i of T items split over G CTAs (contiguous equal ranges).
+__device__ __forceinline__ int64_t owner_of(int64_t i, int64_t T, int64_t G) { return ((i + 1) * G - 1) / T; }
+
+__device__ __forceinline__ void store_out(void *y, q4_dtype yt, int64_t idx, float v)
+{
+    if (yt == Q4_F32)
+        static_cast<float *>(y)[idx] = v;
+    else if (yt == Q4_BF16)
+        static_cast<__nv_bfloat16 *>(y)[idx] = __float2bfloat16_rn(v);
+    else
+        static_cast<__half *>(y)[idx] = __float2half_rn(v);
+}
+
+// F16: activations (and the A operand) are f16, else bf16.  BT: tokens per
+// tile.  CMP: compact tiles (binary16 scale pairs, zero nibbles, 1072 bytes).
+template <bool F16, int BT, bool CMP>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmx, const Args a)
 {
+    using P = Plan<BT>;
+    constexpr int NC = P::NC, X_HALF = P::X_HALF, X_ST = P::X_ST;
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
-    using P = Plan<NARROW>;
-    constexpr int NS = P::NS, NC = P::NC, A_HALF = P::A_HALF, A_ST = P::A_ST, B_ST = P::B_ST;
+    constexpr int NCOL = BT < 64 ? BT : 64;  // columns per rescale thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sA = smem + P::OFF_A;
-    uint8_t *sB = smem + P::OFF_B;
+    uint8_t *sX = smem + P::OFF_X;
     uint8_t *sC = smem + P::OFF_C;
+    float *sScl = reinterpret_cast<float *>(smem + P::OFF_S);  // [NSC][128 rows]
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
-    uint64_t *full = bar, *empty = bar + NS;
-    uint64_t *full_c = empty + NS, *empty_c = full_c + NC;
-    uint64_t *acc_full = empty_c + NC, *acc_empty = acc_full + 2;
-    uint64_t *drain = acc_empty + 2;
+    uint64_t *xfull = bar, *afull = xfull + NS, *empty = afull + NS;
+    uint64_t *cfull = empty + NS, *cempty = cfull + NC;
+    uint64_t *sfull = cempty + NC, *sempty = sfull + NSC;
+    uint64_t *dfull = sempty + NSC, *dempty = dfull + 2, *drain = dempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile unsigned int *bcast = reinterpret_cast<volatile unsigned int *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
     const int ntiles_rows = (a.N + TILE_ROWS - 1) / TILE_ROWS;
-    const int T = a.mt * a.nt;
+    const int64_t T = static_cast<int64_t>(a.mt) * a.nt;
+    const int64_t items = T * NG;
+    Cursor cur0;
+    if (a.split) {
+        cur0.pos = blockIdx.x * items / gridDim.x;
+        cur0.end = (blockIdx.x + 1) * items / gridDim.x;
+    } else {
+        cur0.pos = blockIdx.x;
+        cur0.end = T;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1 + 8);  // activation producer + dequantizing warps
+            mbar_init(&xfull[i], 1);
+            mbar_init(&afull[i], 4);
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < NC; ++i) {
-            mbar_init(&full_c[i], 1);
-            mbar_init(&empty_c[i], 8);
+            mbar_init(&cfull[i], 1);
+            mbar_init(&cempty[i], 4);
+        }
+        for (int i = 0; i < NSC; ++i) {
+            mbar_init(&sfull[i], 4);
+            mbar_init(&sempty[i], 8);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&dfull[i], 1);
+            mbar_init(&dempty[i], 8);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -241,100 +336,92 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------- activation producer
         if (lane == 0) {
-            int is = 0;
+            Cursor cur = cur0;
+            int tile, g0, g1, i = 0;
             bool ok = true;
-            // per 64-k half: one box of bt rows, or two of SUB rows when bt = 256
-            const int nbox = a.bt > SUB ? 2 : 1;
-            const uint32_t st_bytes = 2u * static_cast<uint32_t>(a.bt) * BK * 2;
-            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
-                const int m0 = (tile % a.mt) * a.bt;
-                for (int g = 0; g < NG; ++g) {
-                    const int s = is % NS;
-                    if (is >= NS && !mbar_wait_bounded(&empty[s], ((is / NS) - 1) & 1, abort_flag,
-                                                       a.wait_ns, a.err)) {
+            while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
+                int mb, nb;
+                tile_coords(tile, a.mt, a.nt, mb, nb);
+                for (int g = g0; g < g1; ++g) {
+                    const int s = i % NS;
+                    if (i >= NS && !mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, abort_flag,
+                                                      a.wait_ns, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], st_bytes);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint8_t *dst = sA + s * A_ST + h * A_HALF;
-                        tma_load_2d(dst, &tmx, g * G + h * BK, m0, &full[s]);
-                        if (nbox == 2) tma_load_2d(dst + A_BOX, &tmx, g * G + h * BK, m0 + SUB, &full[s]);
-                    }
-                    ++is;
+                    mbar_arrive_expect_tx(&xfull[s], static_cast<uint32_t>(X_ST));
+                    uint8_t *dst = sX + s * X_ST;
+                    tma_load_2d(dst, &tmx, g * G, mb * BT, &xfull[s]);
+                    tma_load_2d(dst + X_HALF, &tmx, g * G + 64, mb * BT, &xfull[s]);
+                    ++i;
                 }
             }
             // every issued copy lands before the CTA may exit
-            for (int i = max(0, is - NS); i < is; ++i)
-                mbar_wait_bounded(&full[i % NS], (i / NS) & 1, abort_flag, a.wait_ns, a.err, false);
+            for (int j = max(0, i - NS); j < i; ++j)
+                mbar_wait_bounded(&xfull[j % NS], (j / NS) & 1, abort_flag, a.wait_ns, a.err, false);
         }
-    } else if (warp == 14) {
+    } else if (warp == 2) {
         // ----------------------------------------------------- weight producer
-        if (lane == 0) {
-            int ic = 0;
+        if (lane == 0 && !a.debug_no_copy) {
+            Cursor cur = cur0;
+            int tile, g0, g1, i = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
-                const int rt0 = (tile / a.mt) * RT, nrt = min(RT, ntiles_rows - rt0);
-                for (int g = 0; g < NG; ++g) {
-                    const int sc = ic % NC;
-                    if (ic >= NC && !mbar_wait_bounded(&empty_c[sc], ((ic / NC) - 1) & 1, abort_flag,
-                                                       a.wait_ns, a.err)) {
+            while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
+                int mb, nb;
+                tile_coords(tile, a.mt, a.nt, mb, nb);
+                const int rt0 = nb * RT, nrt = min(RT, ntiles_rows - rt0);
+                for (int g = g0; g < g1; ++g) {
+                    const int c = i % NC;
+                    if (i >= NC && !mbar_wait_bounded(&cempty[c], ((i / NC) - 1) & 1, abort_flag,
+                                                      a.wait_ns, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_c[sc], static_cast<uint32_t>(nrt) * TBY);
+                    mbar_arrive_expect_tx(&cfull[c], static_cast<uint32_t>(nrt) * TBY);
                     for (int r = 0; r < nrt; ++r)
-                        bulk_g2s(sC + sc * C_STAGE + r * TBY,
+                        bulk_g2s(sC + c * C_STAGE + r * TBY,
                                  a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TBY, TBY,
-                                 &full_c[sc]);
-                    ++ic;
+                                 &cfull[c]);
+                    ++i;
                 }
             }
-            for (int i = max(0, ic - NC); i < ic; ++i)
-                mbar_wait_bounded(&full_c[i % NC], (i / NC) & 1, abort_flag, a.wait_ns, a.err, false);
+            for (int j = max(0, i - NC); j < i; ++j)
+                mbar_wait_bounded(&cfull[j % NC], (j / NC) & 1, abort_flag, a.wait_ns, a.err, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(F16 ? 0u : 1u, static_cast<uint32_t>(a.bt));
-            int is = 0, tt = 0;
-            bool issued = false, ok = true;
-            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
-                const int buf = tt & 1;
-                if (tt >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((tt >> 1) - 1) & 1, abort_flag,
-                                                  a.wait_ns, a.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d = tmem + buf * 256;
-                for (int g = 0; g < NG; ++g) {
-                    const int s = is % NS;
-                    if (!mbar_wait_bounded(&full[s], (is / NS) & 1, abort_flag, a.wait_ns, a.err)) {
+            const uint32_t idesc = idesc_f16(F16 ? 0u : 1u, static_cast<uint32_t>(BT));
+            Cursor cur = cur0;
+            int tile, g0, g1, i = 0;
+            bool ok = true, issued = false;
+            while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
+                for (int g = g0; g < g1; ++g) {
+                    const int s = i % NS, b = i & 1;
+                    // the MMA thread polls (reacts at once; it has nothing else to do)
+                    if ((i >= 2 && !mbar_wait_bounded(&dempty[b], ((i >> 1) - 1) & 1, abort_flag,
+                                                      a.wait_ns, a.err, true, true)) ||
+                        !mbar_wait_bounded(&afull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err,
+                                           true, true) ||
+                        !mbar_wait_bounded(&xfull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err,
+                                           true, true)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // A operand: the weight tile; B operand: the bt activation
-                    // rows (one TMA box, or two contiguous ones); per 64-k half
-                    // four MMAs of k = 16
-                    const uint32_t xa = smem_u32(sA + s * A_ST);
-                    const uint32_t wb = smem_u32(sB + s * B_ST);
+                    const uint32_t xs = smem_u32(sX + s * X_ST);
+                    const uint32_t d = tmem + static_cast<uint32_t>(b) * 128u;
+                    const uint32_t at = tmem + A_COL + static_cast<uint32_t>(s) * 64u;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int k16 = 0; k16 < BK / 16; ++k16) {
-                            const uint32_t acc = (g > 0 || h > 0 || k16 > 0) ? 1u : 0u;
-                            mma_f16(d, sw128_desc(wb + h * B_HALF + 32 * k16),
-                                    sw128_desc(xa + h * A_HALF + 32 * k16), idesc, acc);
-                        }
+                    for (int k16 = 0; k16 < 8; ++k16)
+                        mma_ts(d, at + 8u * k16,
+                               sw128_desc(xs + (k16 >> 2) * X_HALF + 32 * (k16 & 3)), idesc,
+                               k16 > 0 ? 1u : 0u);
                     issued = true;
                     mma_commit(&empty[s]);
-                    ++is;
+                    mma_commit(&dfull[b]);
+                    ++i;
                 }
-                if (!ok) break;
-                mma_commit(&acc_full[buf]);
             }
             if (issued) {
                 // all issued MMAs complete before tensor memory is freed
@@ -342,114 +429,226 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_wait_bounded(drain, 0, abort_flag, a.wait_ns, a.err, false);
             }
         }
-    } else if (warp < 10) {
-        // ------------------------------------------------------ dequantize
-        const int d = warp - 2, gq = lane >> 2, t = lane & 3;
-        int is = 0, ic = 0;
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------ A operand builders
+        // Thread = weight row R of the tile (tensor-memory lane R).  Its codes
+        // sit in lanes 4 (R % 8) + t of its packed tile (t = 0..3), in the
+        // nibble fields of row R % 16 (tiled layout, include/q4.h): word i of
+        // chunk c of lane 4 (R % 8) + t holds k = 16 (4c + i) + 2t + {0, 1}
+        // and + {8, 9}, i.e. the packed pairs 32c + 8i + t and 32c + 8i + t + 4
+        // of the group's 64.
+        const int q = warp - 4;
+        const int R = 32 * q + lane, d = R >> 4, rr = R & 15;
+        const int lg = 4 * (rr & 7);
+        const uint32_t sA = (rr & 8) ? 4u : 0u, sB = (rr & 8) ? 8u : 12u;
+        const uint32_t MAG = F16 ? 0x64006400u : 0x43004300u;
+        const float OFF = F16 ? 1024.0f : 128.0f;
+        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        Cursor cur = cur0;
+        int tile, g0, g1, i = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
-            const int nb = tile / a.mt;
+        while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
+            int mb, nb;
+            tile_coords(tile, a.mt, a.nt, mb, nb);
             const int nrt = min(RT, ntiles_rows - nb * RT);
-            for (int g = 0; g < NG; ++g) {
-                const int s = is % NS, sc = ic % NC;
-                ok = mbar_wait_bounded(&full_c[sc], (ic / NC) & 1, abort_flag, a.wait_ns, a.err);
-                if (ok && is >= NS)
-                    ok = mbar_wait_bounded(&empty[s], ((is / NS) - 1) & 1, abort_flag, a.wait_ns,
+            const bool live = d < nrt;
+            for (int g = g0; g < g1; ++g) {
+                const int c = i % NC, s = i % NS, sl = i % NSC;
+                ok = mbar_wait_bounded(&cfull[c], (i / NC) & 1, abort_flag, a.wait_ns, a.err);
+                if (ok && i >= NS)
+                    ok = mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, abort_flag, a.wait_ns,
                                            a.err);
+                if (ok && i >= NSC)
+                    ok = mbar_wait_bounded(&sempty[sl], ((i / NSC) - 1) & 1, abort_flag,
+                                           a.wait_ns, a.err);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
-                if (d < nrt) {
-                    const uint8_t *ct = sC + sc * C_STAGE + d * TBY;
-                    float2 sp;
-                    uint32_t z0, z8;
-                    if (CMP) {  // binary16 pair (widened exactly), zero nibbles
-                        sp = __half22float2(*reinterpret_cast<const __half2 *>(ct + SCALE_OFF + 4 * gq));
-                        const uint32_t zb = ct[CMP_ZERO_OFF + gq];
-                        z0 = zb & 0x0Fu;
-                        z8 = zb >> 4;
+                const uint8_t *ct = sC + c * C_STAGE + d * TBY;
+                float sc = 0.0f;
+                uint32_t mz = 0;
+                if (live) {
+                    int z;
+                    if (CMP) {
+                        sc = __half2float(*reinterpret_cast<const __half *>(
+                            ct + SCALE_OFF + 4 * (rr & 7) + 2 * (rr >> 3)));
+                        z = (ct[CMP_ZERO_OFF + (rr & 7)] >> (4 * (rr >> 3))) & 15;
                     } else {
-                        sp = *reinterpret_cast<const float2 *>(ct + SCALE_OFF + 8 * gq);
-                        const uint32_t zp = *reinterpret_cast<const uint16_t *>(ct + ZERO_OFF + 2 * gq);
-                        z0 = zp & 0xFFu;
-                        z8 = zp >> 8;
+                        sc = *reinterpret_cast<const float *>(ct + SCALE_OFF + 8 * (rr & 7) +
+                                                             4 * (rr >> 3));
+                        z = ct[ZERO_OFF + 2 * (rr & 7) + (rr >> 3)];
                     }
-                    const float nz0 = -(128.0f + static_cast<float>(z0));
-                    const float nz8 = -(128.0f + static_cast<float>(z8));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 cw = *reinterpret_cast<const uint4 *>(ct + h * 512 + 16 * lane);
-                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-                        uint8_t *row0 = sB + s * B_ST + h * B_HALF + (16 * d + gq) * 128 + 4 * t;
-                        uint8_t *row8 = row0 + 8 * 128;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t w = words[i];
-                            const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);
-                            const uint32_t p1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
-                            const uint32_t p3 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
-                            const uint32_t p2 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
-                            const int c_lo = ((2 * i) ^ gq) * 16, c_hi = ((2 * i + 1) ^ gq) * 16;
-                            *reinterpret_cast<uint32_t *>(row0 + c_lo) = dequant_pair<F16>(p0, nz0, sp.x);
-                            *reinterpret_cast<uint32_t *>(row0 + c_hi) = dequant_pair<F16>(p2, nz0, sp.x);
-                            *reinterpret_cast<uint32_t *>(row8 + c_lo) = dequant_pair<F16>(p1, nz8, sp.y);
-                            *reinterpret_cast<uint32_t *>(row8 + c_hi) = dequant_pair<F16>(p3, nz8, sp.y);
-                        }
+                    const float nz = -(OFF + static_cast<float>(z));  // exact in 16 bits
+                    if (F16) {
+                        const __half2 h = __floats2half2_rn(nz, nz);
+                        mz = *reinterpret_cast<const uint32_t *>(&h);
+                    } else {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(nz, nz);
+                        mz = *reinterpret_cast<const uint32_t *>(&h);
                     }
                 }
-                fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                sScl[sl * BN + R] = sc;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t v[32];
+                    if (live) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const uint4 w4 =
+                                *reinterpret_cast<const uint4 *>(ct + cc * 512 + 16 * (lg + t));
+                            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int i4 = 0; i4 < 4; ++i4) {
+                                v[8 * i4 + t] =
+                                    sub_pair<F16>(lop3_and_or(ws[i4] >> sA, 0x000F000Fu, MAG), mz);
+                                v[8 * i4 + t + 4] =
+                                    sub_pair<F16>(lop3_and_or(ws[i4] >> sB, 0x000F000Fu, MAG), mz);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;  // rows past the matrix
+                    }
+                    tmem_st32(tlane + A_COL + static_cast<uint32_t>(s) * 64u + 32u * cc, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&full[s]);
-                    mbar_arrive(&empty_c[sc]);
+                    mbar_arrive(&afull[s]);
+                    mbar_arrive(&cempty[c]);
+                    mbar_arrive(&sfull[sl]);
                 }
-                ++is;
-                ++ic;
+                ++i;
             }
         }
-    } else if (warp < 14) {
-        // ------------------------------------------------------ epilogue
-        // Warp p reads tensor-memory lanes 32p..32p+31 (weight rows n0 + 32p
-        // + lane); each 32-column load gives a lane 32 consecutive tokens, and
-        // for every token the warp stores 32 consecutive outputs (64 bytes).
-        const int p = warp & 3;
-        int tt = 0;
+    } else if (warp >= 8) {
+        // ------------------------------------------------ rescale + epilogue
+        const int w = warp - 8, q = w & 3, ch = w >> 2;
+        const bool active = ch * 64 < BT;
+        const int R = 32 * q + lane;
+        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 64u * ch;
+        Cursor cur = cur0;
+        int tile, g0, g1, i = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x, ++tt) {
-            const int m0 = (tile % a.mt) * a.bt, n0 = (tile / a.mt) * BN;
-            const int buf = tt & 1;
-            ok = mbar_wait_bounded(&acc_full[buf], (tt >> 1) & 1, abort_flag, a.wait_ns, a.err);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
+        while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
+            int mb, nb;
+            tile_coords(tile, a.mt, a.nt, mb, nb);
+            const int n = nb * BN + R;
+            float Y[NCOL];
+#pragma unroll
+            for (int j = 0; j < NCOL; ++j) Y[j] = 0.0f;
+            for (int g = g0; g < g1; ++g) {
+                const int b = i & 1, sl = i % NSC;
+                ok = mbar_wait_bounded(&dfull[b], (i >> 1) & 1, abort_flag, a.wait_ns, a.err) &&
+                     mbar_wait_bounded(&sfull[sl], (i / NSC) & 1, abort_flag, a.wait_ns, a.err);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sc = sScl[sl * BN + R];
+                if (active) {
+                    // this thread's NCOL columns in chunks of up to 32; the
+                    // buffer is released as soon as the last chunk is loaded
+                    uint32_t v[32];
+                    if constexpr (NCOL == 16)
+                        tmem_ld16(tlane + static_cast<uint32_t>(b) * 128u, v);
+                    else
+                        tmem_ld32(tlane + static_cast<uint32_t>(b) * 128u, v);
+                    tmem_wait_ld();
+                    if constexpr (NCOL > 32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) Y[j] = fmaf(sc, __uint_as_float(v[j]), Y[j]);
+                        tmem_ld32(tlane + static_cast<uint32_t>(b) * 128u + 32u, v);
+                        tmem_wait_ld();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&dempty[b]);
+                        mbar_arrive(&sempty[sl]);
+                    }
+                    constexpr int J0 = NCOL > 32 ? 32 : 0;
+#pragma unroll
+                    for (int j = 0; j < NCOL - J0; ++j)
+                        Y[J0 + j] = fmaf(sc, __uint_as_float(v[j]), Y[J0 + j]);
+                } else {
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&dempty[b]);
+                        mbar_arrive(&sempty[sl]);
+                    }
+                }
+                ++i;
+            }
+
+            // ---------------------------------------------------- tile output
+            const int64_t first = static_cast<int64_t>(tile) * NG;
+            int c_first = blockIdx.x, nc = 1;
+            if (a.split) {
+                c_first = static_cast<int>(owner_of(first, items, gridDim.x));
+                nc = static_cast<int>(owner_of(first + NG - 1, items, gridDim.x)) - c_first + 1;
+                // every rescale warp decides together whether to go on
+                if (named_barrier_or(1, 256, !ok)) {
+                    ok = false;
+                    break;
+                }
+            } else if (!ok) {
                 break;
             }
-            tc_fence_after();
-            const int n = n0 + 32 * p + lane;
-            uint16_t *ycol = reinterpret_cast<uint16_t *>(a.y) + n;
-#pragma unroll 1
-            for (int c = 0; c < (a.bt + 31) / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * p) << 16) + buf * 256 + 32 * c, v);
-                const int mb = m0 + 32 * c;
-                if (mb >= a.M) break;  // warp-uniform
+            const int m0 = mb * BT + 64 * ch;
+            if (nc == 1) {
+                if (active && n < a.N)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float f = __uint_as_float(v[j]);
-                    uint16_t o;
-                    if (YF16) {
-                        const __half h = __float2half_rn(f);
-                        o = *reinterpret_cast<const uint16_t *>(&h);
-                    } else {
-                        const __nv_bfloat16 bb = __float2bfloat16_rn(f);
-                        o = *reinterpret_cast<const uint16_t *>(&bb);
-                    }
-                    if (mb + j < a.M && n < a.N) ycol[static_cast<int64_t>(mb + j) * a.N] = o;
-                }
+                    for (int j = 0; j < NCOL; ++j)
+                        if (m0 + j < a.M)
+                            store_out(a.y, a.yt, static_cast<int64_t>(m0 + j) * a.N + n, Y[j]);
+                continue;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            // Split tile: publish this CTA's partial, count the arrival; the
+            // last contributor adds all partials in CTA order and clears them.
+            const int64_t slab = static_cast<int64_t>(BN) * BT;
+            float *part = a.partial + (static_cast<int64_t>(tile) * a.maxc * BN + R) * BT + 64 * ch;
+            if (active) {
+                float4 *dst = reinterpret_cast<float4 *>(part + (blockIdx.x - c_first) * slab);
+#pragma unroll
+                for (int j = 0; j < NCOL / 4; ++j)
+                    dst[j] = make_float4(Y[4 * j], Y[4 * j + 1], Y[4 * j + 2], Y[4 * j + 3]);
+            }
+            __threadfence();
+            named_barrier_sync(1, 256);
+            if (w == 0 && lane == 0) *bcast = atomic_add_acq_rel_gpu(&a.count[tile], 1u);
+            named_barrier_sync(1, 256);
+            const unsigned int prev = *bcast;
+            if (prev == static_cast<unsigned int>(nc - 1)) {
+                if (active) {
+                    float v[NCOL];
+#pragma unroll
+                    for (int j = 0; j < NCOL; ++j) v[j] = 0.0f;
+                    for (int cc = 0; cc < nc; ++cc) {
+                        float4 *src = reinterpret_cast<float4 *>(part + cc * slab);
+#pragma unroll
+                        for (int j = 0; j < NCOL / 4; ++j) {
+                            const float4 p = __ldcg(src + j);
+                            v[4 * j] += p.x;
+                            v[4 * j + 1] += p.y;
+                            v[4 * j + 2] += p.z;
+                            v[4 * j + 3] += p.w;
+                        }
+#pragma unroll
+                        for (int j = 0; j < NCOL / 4; ++j) src[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    if (n < a.N)
+#pragma unroll
+                        for (int j = 0; j < NCOL; ++j)
+                            if (m0 + j < a.M)
+                                store_out(a.y, a.yt, static_cast<int64_t>(m0 + j) * a.N + n,
+                                                 v[j]);
+                }
+                if (w == 0 && lane == 0) a.count[tile] = 0u;  // ready for the next call
+            }
         }
     }
 
@@ -489,48 +688,95 @@ static bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+using KernFn = void (*)(CUtensorMap, Args);
+
+template <bool F16, bool CMP>
+static KernFn kernel_for(int bt, int *smem)
+{
+    switch (bt) {
+    case 16: *smem = Plan<16>::SMEM_ALLOC; return k_gemm<F16, 16, CMP>;
+    case 32: *smem = Plan<32>::SMEM_ALLOC; return k_gemm<F16, 32, CMP>;
+    case 64: *smem = Plan<64>::SMEM_ALLOC; return k_gemm<F16, 64, CMP>;
+    default: *smem = Plan<128>::SMEM_ALLOC; return k_gemm<F16, 128, CMP>;
+    }
+}
+
+static int bt_index(int bt) { return bt == 16 ? 0 : bt == 32 ? 1 : bt == 64 ? 2 : 3; }
+
 }  // namespace gm
 
-q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
-                   void *y, q4_dtype yt, int sm_count, unsigned int *err, cudaStream_t s,
-                   cudaError_t *cerr, bool cmp)
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count)
+{
+    using namespace gm;
+    GemmPlan p{};
+    p.bt = 16;
+    while (p.bt < 128 && p.bt < M) p.bt *= 2;
+    p.mt = static_cast<int>((M + p.bt - 1) / p.bt);
+    p.nt = static_cast<int>((N + BN - 1) / BN);
+    const int64_t T = static_cast<int64_t>(p.mt) * p.nt;
+    const int64_t NG = K / G;
+    // Whole tiles in turn when every CTA gets many (the last round costs at
+    // most one tile in eight); otherwise equal ranges of (tile, group) items.
+    p.split = T < 8LL * sm_count && NG > 1;
+    if (!p.split) {
+        p.grid = static_cast<int>(T < sm_count ? T : sm_count);
+        p.maxc = 1;
+        p.workspace = 0;
+        return p;
+    }
+    const int64_t items = T * NG;
+    p.grid = static_cast<int>(items < sm_count ? items : sm_count);
+    int maxc = 1;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t c0 = ((t * NG + 1) * p.grid - 1) / items;
+        const int64_t c1 = (((t + 1) * NG) * p.grid - 1) / items;
+        if (c1 - c0 + 1 > maxc) maxc = static_cast<int>(c1 - c0 + 1);
+    }
+    p.maxc = maxc;
+    if (maxc == 1) {  // no tile is shared: the ranges fall on tile boundaries
+        p.workspace = 0;
+        return p;
+    }
+    const size_t counters = ((static_cast<size_t>(T) * sizeof(unsigned int) + 255) / 256) * 256;
+    p.workspace = counters + static_cast<size_t>(T) * maxc * BN * p.bt * sizeof(float);
+    return p;
+}
+
+q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
+                   const uint8_t *qw, bool cmp, void *y, q4_dtype yt, void *workspace,
+                   unsigned int *err, uint64_t wait_ns, int debug_no_copy, cudaStream_t s,
+                   cudaError_t *cerr)
 {
     using namespace gm;
     *cerr = cudaSuccess;
     const bool f16 = (xt == Q4_F16);
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    int bt = 16;
-    while (bt < BM && bt < M) bt *= 2;
-    const bool narrow = bt <= NARROW_MAX;
     CUtensorMap tmx;
-    if (!make_map(&tmx, x, dt, K, M, K * 2, BK, bt < SUB ? bt : SUB)) return Q4_ERR_UNSUPPORTED;
+    if (!make_map(&tmx, x, dt, K, M, K * 2, 64, p.bt)) return Q4_ERR_UNSUPPORTED;
     Args a{};
-    a.qw = static_cast<const uint8_t *>(qw);
+    a.qw = qw;
     a.y = y;
+    a.yt = yt;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.bt = bt;
-    a.mt = static_cast<int>((M + bt - 1) / bt);
-    a.nt = static_cast<int>((N + BN - 1) / BN);
-    a.wait_ns = 2000000000ull;
+    a.mt = p.mt;
+    a.nt = p.nt;
+    a.split = p.split ? 1 : 0;
+    a.maxc = p.maxc;
+    if (p.workspace > 0) {
+        const int64_t T = static_cast<int64_t>(p.mt) * p.nt;
+        const size_t counters = ((static_cast<size_t>(T) * sizeof(unsigned int) + 255) / 256) * 256;
+        a.count = static_cast<unsigned int *>(workspace);
+        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters);
+    }
+    a.wait_ns = wait_ns;
     a.err = err;
-    const int tiles = a.mt * a.nt;
-    const int grid = tiles < sm_count ? tiles : sm_count;
-    const bool yf16 = (yt == Q4_F16);
-    using KernFn = void (*)(CUtensorMap, Args);
-    static const KernFn kerns[16] = {
-        k_gemm<false, false, false, false>, k_gemm<false, true, false, false>,
-        k_gemm<true, false, false, false>,  k_gemm<true, true, false, false>,
-        k_gemm<false, false, true, false>,  k_gemm<false, true, true, false>,
-        k_gemm<true, false, true, false>,   k_gemm<true, true, true, false>,
-        k_gemm<false, false, false, true>,  k_gemm<false, true, false, true>,
-        k_gemm<true, false, false, true>,   k_gemm<true, true, false, true>,
-        k_gemm<false, false, true, true>,   k_gemm<false, true, true, true>,
-        k_gemm<true, false, true, true>,    k_gemm<true, true, true, true>};
-    const int variant = (cmp ? 8 : 0) + (narrow ? 4 : 0) + (f16 ? 2 : 0) + (yf16 ? 1 : 0);
-    const KernFn kern = kerns[variant];
-    const int smem = narrow ? Plan<true>::SMEM_ALLOC : Plan<false>::SMEM_ALLOC;
+    a.debug_no_copy = debug_no_copy;
+    int smem = 0;
+    const KernFn kern = f16 ? (cmp ? kernel_for<true, true>(p.bt, &smem) : kernel_for<true, false>(p.bt, &smem))
+                            : (cmp ? kernel_for<false, true>(p.bt, &smem) : kernel_for<false, false>(p.bt, &smem));
+    const int variant = (cmp ? 8 : 0) + (f16 ? 4 : 0) + bt_index(p.bt);
     static std::atomic<bool> configured[16][64];  // concurrent first calls may both set it
     int dev = 0;
     cudaGetDevice(&dev);
@@ -539,7 +785,7 @@ q4_status gemm_run(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, 
         if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
         if (dev >= 0 && dev < 64) configured[variant][dev].store(true, std::memory_order_relaxed);
     }
-    kern<<<grid, THREADS, smem, s>>>(tmx, a);
+    kern<<<p.grid, THREADS, smem, s>>>(tmx, a);
     *cerr = cudaGetLastError();
     return *cerr == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }

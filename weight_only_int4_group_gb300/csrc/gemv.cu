@@ -365,8 +365,9 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // held by this CTA alone is written out directly.  Otherwise the partial
     // sums go to this CTA's slot of the workspace and the arrival counter is
     // stepped; the contributor that arrives last sums the partials of all
-    // contributors in CTA order (the same order whoever arrives last) and
-    // resets the counter for the next call.
+    // contributors in CTA order (the same order whoever arrives last), and
+    // clears the partials it read and the counter, so a completed call
+    // leaves the workspace zero for the next one, whatever its shape.
     if (warp == W + 1) {
         // outputs and the workspace may belong to the previous kernel
         grid_dep_wait();
@@ -419,7 +420,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                                     for (int u = 0; u < 4; ++u)
-                                        if (c0 + cc < nc) v[u] += pv[cc][u];
+                                        if (c0 + cc < nc) {
+                                            v[u] += pv[cc][u];
+                                            // consumed: the workspace goes back to zero
+                                            if (i0 + 32 * u < nout)
+                                                part[(c0 + cc) * slab + i0 + 32 * u] = 0.0f;
+                                        }
                             }
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {

@@ -18,8 +18,9 @@
 //     Q4_ERR_UNSUPPORTED before anything is launched;
 //   * all calls on a device share the one array, which keeps the last call's
 //     contents: each call clears the counter block it relies on (an
-//     asynchronous memset on the same stream, no allocation), and calls that
-//     overlap on the GPU (e.g. concurrent streams) race on the array, so
+//     asynchronous memset on the same stream, no allocation; completed calls
+//     leave it zero anyway, this also covers one that timed out), and calls
+//     that overlap on the GPU (e.g. concurrent streams) race on the array, so
 //     callers must order them;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -60,23 +61,30 @@ void *scratch_for_current_device(cudaError_t *err)
 }  // namespace
 
 extern "C" q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K,
-                                     const void *qw, void *y, q4_dtype yt, q4_stream_t stream)
+                                     const void *qw, q4_layout layout, size_t qw_bytes, void *y,
+                                     q4_dtype yt, q4_stream_t stream)
 {
     if (!x || !qw || !y) return Q4_ERR_INVALID_ARG;
     if (N < 1 || K < Q4_GROUP || K % Q4_GROUP != 0) return Q4_ERR_INVALID_ARG;
     if (M < 1 || M > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED;
+    // the weight buffer matches its layout and shape (checked again by q4_gemv)
+    const size_t wb = q4_weight_bytes(N, K, layout);
+    if (wb == 0 || qw_bytes != wb) return Q4_ERR_INVALID_ARG;
     const size_t need = q4_gemv_workspace_bytes(M, N, K);
     if (need > Q4_NOALLOC_SCRATCH_BYTES) return Q4_ERR_UNSUPPORTED;  // beyond the static maximum
     cudaError_t err = cudaSuccess;
     void *scratch = scratch_for_current_device(&err);
-    if (!scratch) return Q4_ERR_CUDA;
+    if (!scratch) return q4::cuda_fail(err);
     if (need > 0) {
         // The arrival counters (one u32 per 32 output rows, padded to 256
-        // bytes, at the start of the workspace) must start at zero.
+        // bytes, at the start of the workspace) must start at zero.  A
+        // completed call leaves them zero; this also covers a call that
+        // ended in a bounded-wait timeout.
         const size_t counters = q4::gemv_counter_bytes(N);
         err = cudaMemsetAsync(scratch, 0, counters < need ? counters : need,
                               reinterpret_cast<cudaStream_t>(stream));
-        if (err != cudaSuccess) return Q4_ERR_CUDA;
+        if (err != cudaSuccess) return q4::cuda_fail(err);
     }
-    return q4_gemv(x, xt, M, N, K, qw, y, yt, need > 0 ? scratch : nullptr, need, stream);
+    return q4_gemv(x, xt, M, N, K, qw, layout, qw_bytes, y, yt, need > 0 ? scratch : nullptr, need,
+                   stream);
 }
