@@ -14,28 +14,38 @@
 // (page "LLM Quantization Architecture in Depth", "Kernels and memory
 // layout").
 //
-// One persistent CTA per SM, 16 warps with fixed roles:
+// One persistent CTA per SM, 19 warps with fixed roles (a warp reaches the
+// tensor-memory lanes of quadrant warp % 4 only):
 //   warp 0      activation producer: X tiles by 2-D tensor TMA (128-byte
 //               swizzle, K-major), one stage per group;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma;
 //   warp 2      weight producer: the group's 8 packed tiles (16 rows each)
 //               by 1-D bulk copies into a ring of code stages;
-//   warp 3      idle;
-//   warps 4-7   operand builders, one per tensor-memory lane quadrant: each
-//               thread owns one weight row, turns its 128 codes into 64
-//               packed (q - zero) pairs with one LOP3 and one packed FMA per
-//               pair, and stores them with tcgen05.st as the MMA's A operand
-//               (tensor memory, not shared memory: shared memory carries only
-//               the activations and the packed codes);
-//   warps 8-15  rescale and epilogue: per group each thread loads its row's
+//   warps 3-10  operand builders, two per tensor-memory lane quadrant (one
+//               per half of the group's k): each thread owns one weight row,
+//               turns its 64 codes into 32 packed (q - zero) pairs with a
+//               shift, one LOP3 and one packed FMA per pair, and stores them
+//               with tcgen05.st as the MMA's A operand (tensor memory, not
+//               shared memory: shared memory carries only the activations and
+//               the packed codes);
+//   warps 11-18 rescale and epilogue, two per quadrant (each half of the
+//               tile's token columns): per group each thread loads its row's
 //               D_g columns (tcgen05.ld), releases the buffer and adds
 //               scale * D_g into its f32 accumulators; at the end of a tile
 //               it stores the row (or a partial sum, below).
-// Tensor memory (512 columns): D_g double-buffered at columns 0 and 128 (128
-// weight rows x up to 128 tokens), A stages of one group at 256 + 64 s.
+// Tensor memory (512 columns): D_g double-buffered in columns [0, 256) and
+// the A stages of one group each at 256 + 64 s.  With at most 64 tokens a
+// group's 8 MMAs alternate between two accumulators (its two k halves,
+// summed by the rescale): an MMA of fewer than 128 columns takes about 51
+// cycles however small, so a single dependent chain of 8 would leave the
+// tensor core idle.
 // A CTA tile is 128 weight rows x BT tokens, BT the smallest of 16, 32, 64,
-// 128 that covers M (128 beyond): one 128 x BT x 16 MMA per 16 k, A from
-// tensor memory, B = the activation rows from shared memory.
+// 128 that covers M (128 beyond): 128 x BT x 16 MMAs, A from tensor memory,
+// B = the activation rows from shared memory.
+// Per group the MMA thread waits for two barriers (its D buffer free, A
+// built and the activations landed -- one operand builder waits for the
+// latter before it arrives) and commits once: that one commit frees the
+// activation and A stage and hands D_g to the rescale warps.
 //
 // Work: when there are many tiles every CTA takes whole tiles in turn; when
 // there are few (a few dozen tokens), the tiles' groups form one sequence of
@@ -60,7 +70,7 @@ namespace gm {
 constexpr int BN = 128;                    // weight rows per tile
 constexpr int RT = BN / TILE_ROWS;         // 8 packed tiles per group
 constexpr int C_STAGE = RT * TILE_BYTES;   // 8832 bytes of codes per group (compact: 8576 used)
-constexpr int THREADS = 512;
+constexpr int THREADS = 608;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL = 256;            // first tensor-memory column of the A stages
 constexpr int NS = 4;                      // activation / A stages
@@ -76,7 +86,7 @@ struct Plan {
     static constexpr int OFF_C = NS * X_ST;
     static constexpr int OFF_S = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;  // scale slots
     static constexpr int OFF_BAR = OFF_S + NSC * BN * 4;
-    static constexpr int NBAR = 3 * NS + 2 * NC + 2 * NSC + 5;
+    static constexpr int NBAR = 3 * NS + 2 * NC + NSC + 3;
     static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
     static_assert(X_HALF % 1024 == 0, "swizzled halves start on 1024-byte boundaries");
@@ -168,17 +178,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// v <- 32 (or 16) consecutive columns of this warp's lanes; completes at tmem_wait_ld.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+// v <- consecutive columns of this warp's lanes; complete at tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8])
 {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : Q4_W8(v, 0), Q4_W8(v, 8), Q4_W8(v, 16), Q4_W8(v, 24)
-        : "r"(taddr)
-        : "memory");
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : Q4_W8(v, 0)
+                 : "r"(taddr)
+                 : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[32])
+__device__ __forceinline__ void tmem_ld16x(uint32_t taddr, uint32_t (&v)[16])
 {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -189,6 +197,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[32])
 }
 #undef Q4_R8
 #undef Q4_W8
+
+// C consecutive 32-bit columns (C = 8 or 16) of this warp's lanes.
+template <int C>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[C])
+{
+    if constexpr (C == 8)
+        tmem_ld8(taddr, v);
+    else
+        tmem_ld16x(taddr, v);
+}
 
 // d = a * 1 + c on a pair of 16-bit floats (bf16 or f16); exact here: a is
 // offset + q, c = -(offset + zero), the difference a small integer.
@@ -275,18 +293,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     using P = Plan<BT>;
     constexpr int NC = P::NC, X_HALF = P::X_HALF, X_ST = P::X_ST;
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
-    constexpr int NCOL = BT < 64 ? BT : 64;  // columns per rescale thread
+    constexpr int NCOL = BT >= 128 ? 64 : BT / 2;  // token columns per rescale thread
+    constexpr int CH = NCOL < 16 ? NCOL : 16;        // columns per tensor-memory load
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sX = smem + P::OFF_X;
     uint8_t *sC = smem + P::OFF_C;
     float *sScl = reinterpret_cast<float *>(smem + P::OFF_S);  // [NSC][128 rows]
+    // xfull: activations landed; afull: A built (8 builders); mdone: the
+    // group's MMAs completed (frees the stage, hands D_g over); cfull/cempty:
+    // code stages; sfull: scales handed over; dempty: D buffer read.
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
-    uint64_t *xfull = bar, *afull = xfull + NS, *empty = afull + NS;
-    uint64_t *cfull = empty + NS, *cempty = cfull + NC;
-    uint64_t *sfull = cempty + NC, *sempty = sfull + NSC;
-    uint64_t *dfull = sempty + NSC, *dempty = dfull + 2, *drain = dempty + 2;
+    uint64_t *xfull = bar, *afull = xfull + NS, *mdone = afull + NS;
+    uint64_t *cfull = mdone + NS, *cempty = cfull + NC;
+    uint64_t *sfull = cempty + NC;
+    uint64_t *dempty = sfull + NSC, *drain = dempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile unsigned int *bcast = reinterpret_cast<volatile unsigned int *>(tmem_slot + 2);
@@ -308,21 +330,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&xfull[i], 1);
-            mbar_init(&afull[i], 4);
-            mbar_init(&empty[i], 1);
+            mbar_init(&afull[i], 8);
+            mbar_init(&mdone[i], 1);
         }
         for (int i = 0; i < NC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], 4);
+            mbar_init(&cempty[i], 8);
         }
-        for (int i = 0; i < NSC; ++i) {
-            mbar_init(&sfull[i], 4);
-            mbar_init(&sempty[i], 8);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&dfull[i], 1);
-            mbar_init(&dempty[i], 8);
-        }
+        for (int i = 0; i < NSC; ++i) mbar_init(&sfull[i], 4);
+        for (int i = 0; i < 2; ++i) mbar_init(&dempty[i], 8);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -344,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tile_coords(tile, a.mt, a.nt, mb, nb);
                 for (int g = g0; g < g1; ++g) {
                     const int s = i % NS;
-                    if (i >= NS && !mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, abort_flag,
+                    if (i >= NS && !mbar_wait_bounded(&mdone[s], ((i / NS) - 1) & 1, abort_flag,
                                                       a.wait_ns, a.err)) {
                         ok = false;
                         break;
@@ -396,31 +412,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             int tile, g0, g1, i = 0;
             bool ok = true, issued = false;
             while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
-                for (int g = g0; g < g1; ++g) {
+                for (int g = g0; g < g1; ++g, ++i) {
                     const int s = i % NS, b = i & 1;
                     // the MMA thread polls (reacts at once; it has nothing else to do)
                     if ((i >= 2 && !mbar_wait_bounded(&dempty[b], ((i >> 1) - 1) & 1, abort_flag,
                                                       a.wait_ns, a.err, true, true)) ||
                         !mbar_wait_bounded(&afull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err,
-                                           true, true) ||
-                        !mbar_wait_bounded(&xfull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err,
                                            true, true)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t xs = smem_u32(sX + s * X_ST);
-                    const uint32_t d = tmem + static_cast<uint32_t>(b) * 128u;
                     const uint32_t at = tmem + A_COL + static_cast<uint32_t>(s) * 64u;
+                    if constexpr (BT <= 64) {
+                        // two accumulators (k halves 0-63 and 64-127), interleaved
+                        const uint32_t d0 = tmem + static_cast<uint32_t>(b) * 128u;
 #pragma unroll
-                    for (int k16 = 0; k16 < 8; ++k16)
-                        mma_ts(d, at + 8u * k16,
-                               sw128_desc(xs + (k16 >> 2) * X_HALF + 32 * (k16 & 3)), idesc,
-                               k16 > 0 ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k) {
+                            mma_ts(d0, at + 8u * k, sw128_desc(xs + 32 * k), idesc, k > 0 ? 1u : 0u);
+                            mma_ts(d0 + 64u, at + 32u + 8u * k, sw128_desc(xs + X_HALF + 32 * k),
+                                   idesc, k > 0 ? 1u : 0u);
+                        }
+                    } else {
+                        const uint32_t d = tmem + static_cast<uint32_t>(b) * 128u;
+#pragma unroll
+                        for (int k16 = 0; k16 < 8; ++k16)
+                            mma_ts(d, at + 8u * k16,
+                                   sw128_desc(xs + (k16 >> 2) * X_HALF + 32 * (k16 & 3)), idesc,
+                                   k16 > 0 ? 1u : 0u);
+                    }
                     issued = true;
-                    mma_commit(&empty[s]);
-                    mma_commit(&dfull[b]);
-                    ++i;
+                    mma_commit(&mdone[s]);
                 }
             }
             if (issued) {
@@ -429,21 +452,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_wait_bounded(drain, 0, abort_flag, a.wait_ns, a.err, false);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 3 && warp < 11) {
         // ------------------------------------------------ A operand builders
-        // Thread = weight row R of the tile (tensor-memory lane R).  Its codes
-        // sit in lanes 4 (R % 8) + t of its packed tile (t = 0..3), in the
-        // nibble fields of row R % 16 (tiled layout, include/q4.h): word i of
-        // chunk c of lane 4 (R % 8) + t holds k = 16 (4c + i) + 2t + {0, 1}
-        // and + {8, 9}, i.e. the packed pairs 32c + 8i + t and 32c + 8i + t + 4
+        // Thread = weight row R of the tile (tensor-memory lane R); builder
+        // warp w (w % 4 = q) builds k half (w - 3) / 4 of lane quadrant q.  The row's codes sit
+        // in lanes 4 (R % 8) + t of its packed tile (t = 0..3), in the nibble
+        // fields of row R % 16 (tiled layout, include/q4.h): word i of chunk
+        // h of lane 4 (R % 8) + t holds k = 16 (4h + i) + 2t + {0, 1} and
+        // + {8, 9}, i.e. the packed pairs 32h + 8i + t and 32h + 8i + t + 4
         // of the group's 64.
-        const int q = warp - 4;
+        const int q = warp & 3, kh = (warp - 3) >> 2;
         const int R = 32 * q + lane, d = R >> 4, rr = R & 15;
         const int lg = 4 * (rr & 7);
         const uint32_t sA = (rr & 8) ? 4u : 0u, sB = (rr & 8) ? 8u : 12u;
         const uint32_t MAG = F16 ? 0x64006400u : 0x43004300u;
         const float OFF = F16 ? 1024.0f : 128.0f;
-        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16) + A_COL + 32u * kh;
         Cursor cur = cur0;
         int tile, g0, g1, i = 0;
         bool ok = true;
@@ -454,22 +478,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool live = d < nrt;
             for (int g = g0; g < g1; ++g) {
                 const int c = i % NC, s = i % NS, sl = i % NSC;
+                // A stage s and scale slot sl are free once the MMAs of group
+                // i - NS completed: those waited for the rescale of group
+                // i - NS - 2 to release its D buffer, after it had read its
+                // scale slot, and slot sl's previous user, group i - NSC, is
+                // older still.
                 ok = mbar_wait_bounded(&cfull[c], (i / NC) & 1, abort_flag, a.wait_ns, a.err);
                 if (ok && i >= NS)
-                    ok = mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, abort_flag, a.wait_ns,
+                    ok = mbar_wait_bounded(&mdone[s], ((i / NS) - 1) & 1, abort_flag, a.wait_ns,
                                            a.err);
-                if (ok && i >= NSC)
-                    ok = mbar_wait_bounded(&sempty[sl], ((i / NSC) - 1) & 1, abort_flag,
-                                           a.wait_ns, a.err);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 const uint8_t *ct = sC + c * C_STAGE + d * TBY;
-                float sc = 0.0f;
                 uint32_t mz = 0;
                 if (live) {
                     int z;
+                    float sc;
                     if (CMP) {
                         sc = __half2float(*reinterpret_cast<const __half *>(
                             ct + SCALE_OFF + 4 * (rr & 7) + 2 * (rr >> 3)));
@@ -479,6 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                              4 * (rr >> 3));
                         z = ct[ZERO_OFF + 2 * (rr & 7) + (rr >> 3)];
                     }
+                    if (kh == 0) sScl[sl * BN + R] = sc;
                     const float nz = -(OFF + static_cast<float>(z));  // exact in 16 bits
                     if (F16) {
                         const __half2 h = __floats2half2_rn(nz, nz);
@@ -487,48 +514,51 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const __nv_bfloat162 h = __floats2bfloat162_rn(nz, nz);
                         mz = *reinterpret_cast<const uint32_t *>(&h);
                     }
+                } else if (kh == 0) {
+                    sScl[sl * BN + R] = 0.0f;
                 }
-                sScl[sl * BN + R] = sc;
+                uint32_t v[32];
+                if (live) {
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t v[32];
-                    if (live) {
+                    for (int t = 0; t < 4; ++t) {
+                        const uint4 w4 = *reinterpret_cast<const uint4 *>(ct + kh * 512 + 16 * (lg + t));
+                        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const uint4 w4 =
-                                *reinterpret_cast<const uint4 *>(ct + cc * 512 + 16 * (lg + t));
-                            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                            for (int i4 = 0; i4 < 4; ++i4) {
-                                v[8 * i4 + t] =
-                                    sub_pair<F16>(lop3_and_or(ws[i4] >> sA, 0x000F000Fu, MAG), mz);
-                                v[8 * i4 + t + 4] =
-                                    sub_pair<F16>(lop3_and_or(ws[i4] >> sB, 0x000F000Fu, MAG), mz);
-                            }
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            v[8 * i4 + t] = sub_pair<F16>(lop3_and_or(ws[i4] >> sA, 0x000F000Fu, MAG), mz);
+                            v[8 * i4 + t + 4] = sub_pair<F16>(lop3_and_or(ws[i4] >> sB, 0x000F000Fu, MAG), mz);
                         }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;  // rows past the matrix
                     }
-                    tmem_st32(tlane + A_COL + static_cast<uint32_t>(s) * 64u + 32u * cc, v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;  // rows past the matrix
                 }
+                tmem_st32(tlane + static_cast<uint32_t>(s) * 64u, v);
                 tmem_wait_st();
                 tc_fence_before();
+                // one builder also waits for the stage's activations, so that
+                // A built = everything the MMAs of group i read is in place
+                bool landed = true;
+                if (warp == 3)
+                    landed = mbar_wait_bounded(&xfull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err);
                 __syncwarp();
+                if (!__all_sync(0xffffffffu, landed)) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) {
                     mbar_arrive(&afull[s]);
                     mbar_arrive(&cempty[c]);
-                    mbar_arrive(&sfull[sl]);
+                    if (kh == 0) mbar_arrive(&sfull[sl]);
                 }
                 ++i;
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 11) {
         // ------------------------------------------------ rescale + epilogue
-        const int w = warp - 8, q = w & 3, ch = w >> 2;
-        const bool active = ch * 64 < BT;
+        const int w = warp - 11, q = warp & 3, ch = w >> 2;
         const int R = 32 * q + lane;
-        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 64u * ch;
+        const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(NCOL * ch);
         Cursor cur = cur0;
         int tile, g0, g1, i = 0;
         bool ok = true;
@@ -540,8 +570,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < NCOL; ++j) Y[j] = 0.0f;
             for (int g = g0; g < g1; ++g) {
-                const int b = i & 1, sl = i % NSC;
-                ok = mbar_wait_bounded(&dfull[b], (i >> 1) & 1, abort_flag, a.wait_ns, a.err) &&
+                const int s = i % NS, b = i & 1, sl = i % NSC;
+                ok = mbar_wait_bounded(&mdone[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err) &&
                      mbar_wait_bounded(&sfull[sl], (i / NSC) & 1, abort_flag, a.wait_ns, a.err);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -549,36 +579,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const float sc = sScl[sl * BN + R];
-                if (active) {
-                    // this thread's NCOL columns in chunks of up to 32; the
-                    // buffer is released as soon as the last chunk is loaded
-                    uint32_t v[32];
-                    if constexpr (NCOL == 16)
-                        tmem_ld16(tlane + static_cast<uint32_t>(b) * 128u, v);
-                    else
-                        tmem_ld32(tlane + static_cast<uint32_t>(b) * 128u, v);
+                const uint32_t db = tlane + static_cast<uint32_t>(b) * 128u;
+                // this thread's NCOL columns, CH at a time (with at most 64
+                // tokens also the second k half's accumulator, 64 columns
+                // on); the buffer is released once the last chunk is loaded
+#pragma unroll
+                for (int c0 = 0; c0 < NCOL; c0 += CH) {
+                    uint32_t v[CH], u[CH];
+                    tmem_ld<CH>(db + c0, v);
+                    if constexpr (BT <= 64) tmem_ld<CH>(db + 64u + c0, u);
                     tmem_wait_ld();
-                    if constexpr (NCOL > 32) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) Y[j] = fmaf(sc, __uint_as_float(v[j]), Y[j]);
-                        tmem_ld32(tlane + static_cast<uint32_t>(b) * 128u + 32u, v);
-                        tmem_wait_ld();
+                    if (c0 + CH == NCOL) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&dempty[b]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&dempty[b]);
-                        mbar_arrive(&sempty[sl]);
-                    }
-                    constexpr int J0 = NCOL > 32 ? 32 : 0;
 #pragma unroll
-                    for (int j = 0; j < NCOL - J0; ++j)
-                        Y[J0 + j] = fmaf(sc, __uint_as_float(v[j]), Y[J0 + j]);
-                } else {
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&dempty[b]);
-                        mbar_arrive(&sempty[sl]);
+                    for (int j = 0; j < CH; ++j) {
+                        const float dv = BT <= 64 ? __uint_as_float(v[j]) + __uint_as_float(u[j])
+                                                  : __uint_as_float(v[j]);
+                        Y[c0 + j] = fmaf(sc, dv, Y[c0 + j]);
                     }
                 }
                 ++i;
@@ -598,9 +618,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else if (!ok) {
                 break;
             }
-            const int m0 = mb * BT + 64 * ch;
+            const int m0 = mb * BT + NCOL * ch;
             if (nc == 1) {
-                if (active && n < a.N)
+                if (n < a.N)
 #pragma unroll
                     for (int j = 0; j < NCOL; ++j)
                         if (m0 + j < a.M)
@@ -610,8 +630,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Split tile: publish this CTA's partial, count the arrival; the
             // last contributor adds all partials in CTA order and clears them.
             const int64_t slab = static_cast<int64_t>(BN) * BT;
-            float *part = a.partial + (static_cast<int64_t>(tile) * a.maxc * BN + R) * BT + 64 * ch;
-            if (active) {
+            float *part = a.partial + (static_cast<int64_t>(tile) * a.maxc * BN + R) * BT + NCOL * ch;
+            {
                 float4 *dst = reinterpret_cast<float4 *>(part + (blockIdx.x - c_first) * slab);
 #pragma unroll
                 for (int j = 0; j < NCOL / 4; ++j)
@@ -623,8 +643,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             named_barrier_sync(1, 256);
             const unsigned int prev = *bcast;
             if (prev == static_cast<unsigned int>(nc - 1)) {
-                if (active) {
-                    float v[NCOL];
+                {
+                    // this CTA's own partial is in the workspace too: Y is free
+                    float *v = Y;
 #pragma unroll
                     for (int j = 0; j < NCOL; ++j) v[j] = 0.0f;
                     for (int cc = 0; cc < nc; ++cc) {
