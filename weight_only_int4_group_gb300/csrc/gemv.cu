@@ -54,6 +54,14 @@
 //     activations come from one extra MMA per k-step with an all-ones A
 //     operand.  Per group, y += scale * (D - (offset + zero) * sum x).
 //
+//   Row-split MMA (2 <= M <= 16, bf16/f16 activations): consumer warp w
+//     takes row tiles w * RB/4 .. of every step, all 4 groups, so a row
+//     block needs no reduction across warps and a warp keeps 4x fewer
+//     accumulators; the step's activation rows (up to 16) are staged with
+//     the tiles and read as B fragments with ldmatrix (rows padded by 16
+//     bytes: conflict-free), the group sums come from one all-ones MMA per
+//     k-step and batch tile, shared by the warp's row tiles.
+//
 // Both consumers read 1104-byte tiles (f32 scales, u8 zeros); the tensor-core
 // one also reads compact 1072-byte tiles (binary16 scales widened exactly,
 // zero nibbles; the format the page "Weight quantization" counts as 16-bit
@@ -66,8 +74,8 @@
 namespace q4 {
 
 constexpr int W = 4;        // consumer warps = groups per step
-constexpr int RB = 8;       // row tiles per row block (RB_SMALL for small problems)
-constexpr int RB_SMALL = 2;
+constexpr int RB = 8;       // row tiles per row block (RB_SMALL_ROWS for small problems)
+constexpr int RB_SMALL_ROWS = 4;  // small problems, row-split consumers (one tile per warp)
 constexpr int NSTAGE = 2;   // ring depth (3 for the M = 1 tensor-core kernel on long runs)
 constexpr int THREADS = (W + 2) * 32;  // consumers, producer, epilogue
 constexpr int CONSUMERS = W * 32;
@@ -102,6 +110,9 @@ __host__ __device__ constexpr int smem_bytes(int mode, int xrows, int ms, int ns
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_FMA, 0, 1) + 1024) <= 228 * 1024, "two FMA CTAs per SM");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 8, 8) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 0, 16) + 1024) <= 228 * 1024, "two MMA CTAs per SM");
+static_assert(MIN_BLOCKS * (NSTAGE * stage_bytes(PATH_MMA, 16) + CTRL_BYTES + RB * 16 * 16 * 4 + 1024) <=
+                  228 * 1024,
+              "two row-split CTAs per SM at M = 16");
 static_assert(MIN_BLOCKS * (smem_bytes(PATH_MMA, 1, 1, 3) + 1024) <= 228 * 1024,
               "two 3-stage M = 1 MMA CTAs per SM");
 
@@ -131,6 +142,17 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory; thread 8i + r gives row r of
+// matrix i, and thread 4g + t receives elements (g, 2t) and (g, 2t + 1) of
+// each: with the activation rows as matrix rows these are B fragments.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                            const void *row_addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(row_addr)));
 }
 
 template <int ABT>
@@ -240,19 +262,163 @@ __device__ __forceinline__ void tile_meta(const uint8_t *tile, int gq, float2 &s
     }
 }
 
+
+// Row-split consumer loop (see the file header): warp w accumulates row tiles
+// TPW w .. TPW w + TPW - 1 of each row block over all W groups of a step.
+template <int NT, int ABT, int NSTG, int RBT, bool CMP>
+__device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, int SB, uint64_t *full,
+                                             uint64_t *empty, uint64_t *ofull, uint64_t *ofree,
+                                             volatile int *abort_flag, float *out, int64_t beg,
+                                             int64_t end, int NS, int ntiles, int NG)
+{
+    constexpr int RB = RBT, TPW = RBT / W;
+    constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
+    constexpr int TILES_BYTES = RBT * W * TBY;
+    const uint32_t MAG = ABT == 0 ? 0x43004300u : 0x64006400u;
+    const uint32_t ONES = ABT == 0 ? 0x3F803F80u : 0x3C003C00u;
+    const float OFF = ABT == 0 ? 128.0f : 1024.0f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, t = lane & 3;
+    const int M = a.M;
+    // ldmatrix: this lane gives row (token) lm_tok of matrix lm_mat; matrix
+    // i holds k = 16 (j + i / 2) + 8 (i % 2) .. + 7 of k-step pair (j, j + 1)
+    const int lm_tok = lane & 7, lm_mat = lane >> 3;
+    int xoff[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int tok = min(8 * n + lm_tok, M - 1);  // rows past M: never stored
+        xoff[n] = tok * XROW + (16 * (lm_mat >> 1) + 8 * (lm_mat & 1)) * 2;
+    }
+    float yacc[TPW][NT][4];
+    int gstep = 0, nepi = 0;
+    int rb = static_cast<int>(beg / NS), s = static_cast<int>(beg % NS) - 1;
+    for (int64_t it = beg; it < end; ++it, ++gstep) {
+        if (++s == NS) {
+            s = 0;
+            ++rb;
+        }
+        const int slot = gstep % NSTG;
+        const int nrt = min(RB, ntiles - rb * RB);
+        if (it == beg || s == 0) {
+#pragma unroll
+            for (int r = 0; r < TPW; ++r)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) yacc[r][n][e] = 0.0f;
+        }
+        const bool ok = mbar_wait_bounded(&full[slot], (gstep / NSTG) & 1, abort_flag, a.wait_ns, a.err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        const uint8_t *stage = ring + slot * SB;
+        const uint8_t *xs = stage + TILES_BYTES;
+#pragma unroll 1
+        for (int gi = 0; gi < W; ++gi) {
+            if (s * W + gi >= NG) break;  // the last step may hold fewer groups
+            // B fragments of the group's 8 k-steps for every batch tile
+            uint32_t bf[NT][8][2];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    ldmatrix_x4(bf[n][2 * jj][0], bf[n][2 * jj][1], bf[n][2 * jj + 1][0],
+                                bf[n][2 * jj + 1][1], xs + xoff[n] + gi * G * 2 + jj * 64);
+            // group sums of the activations (all-ones A), one MMA per k-step
+            float S[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S[n][e] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, bf[n][j][0], bf[n][j][1]);
+#pragma unroll
+            for (int r = 0; r < TPW; ++r) {
+                const int tr = warp * TPW + r;
+                if (tr >= nrt) break;  // warp-uniform: tiles past the matrix
+                const uint8_t *tile = stage + (tr * W + gi) * TBY;
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
+                float2 sp;
+                uint32_t zp;
+                tile_meta<CMP>(tile, gq, sp, zp);
+                const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                float d[NT][4];
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d[n][e] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t w = wv[j];
+                    if (NT == 1) {
+                        mma_word<ABT>(d[0], w, bf[0][j][0], bf[0][j][1]);
+                    } else {
+                        const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
+                        const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
+                        const uint32_t a3 = lop3_and_or(w >> 8, 0x000F000Fu, MAG);
+                        const uint32_t a2 = lop3_and_or(w >> 12, 0x000F000Fu, MAG);
+#pragma unroll
+                        for (int n = 0; n < NT; ++n)
+                            mma_ab<ABT>(d[n], a0, a1, a2, a3, bf[n][j][0], bf[n][j][1]);
+                    }
+                }
+                // OFF + zero: the byte under the exponent of 2^23
+                const float zg = __uint_as_float(__byte_perm(zp, 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
+                const float zg8 = __uint_as_float(__byte_perm(zp, 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float *ya = yacc[r][n];
+                    ya[0] = fmaf(sp.x, fmaf(-zg, S[n][0], d[n][0]), ya[0]);
+                    ya[1] = fmaf(sp.x, fmaf(-zg, S[n][1], d[n][1]), ya[1]);
+                    ya[2] = fmaf(sp.y, fmaf(-zg8, S[n][0], d[n][2]), ya[2]);
+                    ya[3] = fmaf(sp.y, fmaf(-zg8, S[n][1], d[n][3]), ya[3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+
+        if (!(it == end - 1 || s == NS - 1)) continue;
+
+        // ----------------------------- this CTA's share of row block rb is done
+        // The hand-off buffer is free once the epilogue warp has finished the
+        // previous row block; the barrier makes the decision uniform.
+        const bool stuck = nepi > 0 && !mbar_wait_bounded(ofree, (nepi - 1) & 1, abort_flag,
+                                                          a.wait_ns, a.err);
+        if (named_barrier_or(1, CONSUMERS, stuck)) return;
+#pragma unroll
+        for (int r = 0; r < TPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = (warp * TPW + r) * 16 + gq + ((e & 2) ? 8 : 0);
+                    const int m = 8 * n + 2 * t + (e & 1);
+                    if (m < M) out[m * (RB * 16) + row] = yacc[r][n][e];  // [m][RB * 16 rows]
+                }
+        named_barrier_sync(1, CONSUMERS);  // out complete before the arrival publishes it
+        if (threadIdx.x == 0) mbar_arrive(ofull);
+        ++nepi;
+    }
+}
+
 // ABT: 0 = bf16 operands (magic 128 + q), 1 = f16 operands (magic 1024 + q).
 // XSPLIT: f32 activations carried as bf16 hi + bf16 lo (two MMAs per step).
 // ONE: M = 1 known at compile time (unused MMA columns skipped).
 // RBT: row tiles per row block.
 // CMP: compact tiles (binary16 scales, 4-bit zeros; tensor-core path only).
-template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE, int RBT, bool CMP>
+// ROWS: row-split consumers (2 <= M <= 16, 16-bit activations staged).
+template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG, bool ONE, int RBT, bool CMP, bool ROWS>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
 {
     constexpr int RB = RBT;
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     static_assert(!(CMP && MODE == PATH_FMA), "compact tiles: tensor-core path only");
+    static_assert(!ROWS || (MODE == PATH_MMA && !XSPLIT && !ONE && RBT % W == 0), "row split");
     constexpr int TILES_BYTES = RBT * W * TBY;
-    constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1 || ROWS) && !XSPLIT;
     // XS32: M = 1 f32 activations staged as f32 with the tiles (split into
     // bf16 hi + lo per step); the FMA path stages the same way
     constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
@@ -268,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     float *after = reinterpret_cast<float *>(smem + NSTG * SB + CTRL_BYTES);
     float *red = (MODE == PATH_FMA) ? after + W * WARP_PAIR_FLOATS : after;
     const int MSR = (MODE == PATH_FMA || ONE) ? 1 : a.M;  // red row stride
-    float *out = red + W * RB * 16 * MSR;          // [RB * 16 rows][M]
+    float *out = red + (ROWS ? 0 : W * RB * 16 * MSR);  // [M][RB * 16 rows], 16-byte aligned
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NG = a.K / G;
@@ -361,19 +527,23 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     }
 
     // ------------------------------------------------------------ epilogue
-    // One hand-off per row block this CTA touches, in order.  A row block
-    // held by this CTA alone is written out directly.  Otherwise the partial
-    // sums go to this CTA's slot of the workspace and the arrival counter is
+    // One hand-off per row block this CTA touches, in order; the hand-off
+    // buffer holds it batch row by batch row, [m][RB * 16 rows], so stores
+    // to y are coalesced along the rows.  A row block held by this CTA alone
+    // is written out directly.  Otherwise the partial sums go to this CTA's
+    // slot of the workspace (16-byte copies) and the arrival counter is
     // stepped; the contributor that arrives last sums the partials of all
-    // contributors in CTA order (the same order whoever arrives last), and
-    // clears the partials it read and the counter, so a completed call
-    // leaves the workspace zero for the next one, whatever its shape.
+    // contributors in CTA order (the same order whoever arrives last; four
+    // 16-byte loads per contributor in flight per lane), and clears the
+    // partials it read and the counter, so a completed call leaves the
+    // workspace zero for the next one, whatever its shape.
     if (warp == W + 1) {
         // outputs and the workspace may belong to the previous kernel
         grid_dep_wait();
         if (beg < end) {
+            constexpr int R16 = RB * 16;
             const int Mo = (MODE == PATH_FMA || ONE) ? 1 : a.M;
-            const int64_t slab = static_cast<int64_t>(RB * 16) * a.M;  // one contributor's partial
+            const int64_t slab4 = static_cast<int64_t>(R16 / 4) * Mo;  // one partial, in float4
             const int rb_first = static_cast<int>(beg / NS), rb_last = static_cast<int>((end - 1) / NS);
             for (int rb = rb_first, e = 0; rb <= rb_last; ++rb, ++e) {
                 const bool ok = mbar_wait_bounded(ofull, e & 1, abort_flag, a.wait_ns, a.err);
@@ -382,58 +552,66 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 const int c_first = static_cast<int>(owner_of(first_item, T, Gc));
                 const int c_last = static_cast<int>(owner_of(first_item + NS - 1, T, Gc));
                 const int nc = c_last - c_first + 1;
-                const int nout = min(RB, ntiles - rb * RB) * 16 * Mo;
-                const int row0 = rb * RB * TILE_ROWS;
+                const int row0 = rb * R16;
+                const int nval = min(min(RB, ntiles - rb * RB) * 16, a.N - row0);  // rows that exist
                 if (nc == 1) {
-                    for (int i = lane; i < nout; i += 32) {
-                        const int row = i / Mo, m = i % Mo;
-                        if (row0 + row < a.N)
+                    for (int i = lane; i < Mo * R16; i += 32) {
+                        const int m = i / R16, row = i % R16;
+                        if (row < nval)
                             store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
                     }
                 } else {
-                    float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
-                    for (int i = lane; i < nout; i += 32)
-                        part[(blockIdx.x - c_first) * slab + i] = out[i];
+                    float4 *part = reinterpret_cast<float4 *>(a.partial) + (static_cast<int64_t>(rb) * a.maxc) * slab4;
+                    float4 *mine = part + (blockIdx.x - c_first) * slab4;
+                    const float4 *o4 = reinterpret_cast<const float4 *>(out);
+                    for (int i = lane; i < slab4; i += 32) mine[i] = o4[i];
                     __syncwarp();
                     unsigned int prev = 0;
                     if (lane == 0) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
                     prev = __shfl_sync(0xffffffffu, prev, 0);
                     __syncwarp();
                     if (prev == static_cast<unsigned int>(nc - 1)) {
-                        // last to arrive: every partial is visible.  Four
-                        // outputs x four contributors of loads in flight at
-                        // once; the sums still run in CTA order.
-                        for (int i0 = lane; i0 < nout; i0 += 4 * 32) {
-                            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        // last to arrive: every partial is visible
+                        for (int i0 = lane; i0 < slab4; i0 += 4 * 32) {
+                            float4 v[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                             for (int c0 = 0; c0 < nc; c0 += 4) {
-                                float pv[4][4];
+                                float4 pv[4][4];
 #pragma unroll
                                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                                     for (int u = 0; u < 4; ++u) {
-                                        const int i = i0 + 32 * u;
-                                        pv[cc][u] = (c0 + cc < nc && i < nout)
-                                                        ? __ldcg(&part[(c0 + cc) * slab + i])
-                                                        : 0.0f;
+                                        const int64_t i = i0 + 32 * u;
+                                        pv[cc][u] = (c0 + cc < nc && i < slab4)
+                                                        ? __ldcg(&part[(c0 + cc) * slab4 + i])
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                                     }
 #pragma unroll
                                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                                    for (int u = 0; u < 4; ++u)
-                                        if (c0 + cc < nc) {
-                                            v[u] += pv[cc][u];
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int64_t i = i0 + 32 * u;
+                                        if (c0 + cc < nc && i < slab4) {
+                                            v[u].x += pv[cc][u].x;
+                                            v[u].y += pv[cc][u].y;
+                                            v[u].z += pv[cc][u].z;
+                                            v[u].w += pv[cc][u].w;
                                             // consumed: the workspace goes back to zero
-                                            if (i0 + 32 * u < nout)
-                                                part[(c0 + cc) * slab + i0 + 32 * u] = 0.0f;
+                                            part[(c0 + cc) * slab4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
                                         }
+                                    }
                             }
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
                                 const int i = i0 + 32 * u;
-                                if (i >= nout) continue;
-                                const int row = i / Mo, m = i % Mo;
-                                if (row0 + row < a.N)
-                                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v[u]);
+                                if (i >= slab4) continue;
+                                const int m = (4 * i) / R16, row = (4 * i) % R16;
+                                const int64_t yb = static_cast<int64_t>(m) * a.N + row0 + row;
+                                if (row < nval) store_y(a.y, a.yt, yb, v[u].x);
+                                if (row + 1 < nval) store_y(a.y, a.yt, yb + 1, v[u].y);
+                                if (row + 2 < nval) store_y(a.y, a.yt, yb + 2, v[u].z);
+                                if (row + 3 < nval) store_y(a.y, a.yt, yb + 3, v[u].w);
                             }
                         }
                         if (lane == 0) a.count[rb] = 0u;  // ready for the next call
@@ -450,6 +628,10 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // Activations may belong to the previous kernel on the stream: touch
     // them only after it has completed.
     grid_dep_wait();
+    if constexpr (ROWS) {
+        consume_rows<NT, ABT, NSTG, RBT, CMP>(a, ring, SB, full, empty, ofull, ofree, abort_flag,
+                                               out, beg, end, NS, ntiles, NG);
+    } else {
     const int gq = lane >> 2, t = lane & 3;
     const int M = ONE ? 1 : a.M;
     const int MS = MSR;
@@ -767,13 +949,13 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             break;
         }
         {
-            const int nout = nrt * 16 * Mo;
-            for (int i = threadIdx.x; i < nout; i += CONSUMERS) {
-                const int row = i / Mo, m = i % Mo;
+            const int nrows = nrt * 16;
+            for (int i = threadIdx.x; i < nrows * Mo; i += CONSUMERS) {
+                const int m = i / nrows, row = i % nrows;
                 float v = 0.0f;
 #pragma unroll
                 for (int w = 0; w < W; ++w) v += red[(w * RB * 16 + row) * MS + m];
-                out[i] = v;
+                out[m * (RB * 16) + row] = v;  // hand-off layout [m][RB * 16 rows]
             }
         }
         // red is reused by the next row block; the arrival publishes out
@@ -781,13 +963,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         if (threadIdx.x == 0) mbar_arrive(ofull);
         ++nepi;
     }
+    }  // !ROWS
 }
 
 // -------------------------------------------------------------------- host
 template <int MODE, int NT, int ABT, bool XSPLIT, int NSTG = NSTAGE, bool ONE = false, int RBT = RB,
-          bool CMP = false>
+          bool CMP = false, bool ROWS = false>
 struct Kern {
-    static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1) && !XSPLIT;
+    static constexpr bool XSTAGED = (MODE == PATH_MMA) && (NT == 1 || ROWS) && !XSPLIT;
     static constexpr bool XS32 = (MODE == PATH_MMA) && XSPLIT && ONE;
     static constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     static int smem(int M)
@@ -795,6 +978,8 @@ struct Kern {
         if (XS32)  // f32 staging as in the FMA path, MMA-sized reduction buffers
             return NSTG * stage_bytes(PATH_FMA, 0, RBT, TBY) + CTRL_BYTES + W * RBT * 16 * 4 +
                    RBT * 16 * 4;
+        if (ROWS)  // staged rows, no cross-warp reduction buffer
+            return NSTG * stage_bytes(MODE, M, RBT, TBY) + CTRL_BYTES + RBT * 16 * M * 4;
         return smem_bytes(MODE, XSTAGED ? M : 0, MODE == PATH_FMA ? 1 : M, NSTG, RBT, TBY);
     }
     static cudaError_t configure(int dev, int M, int *blocks_per_sm)
@@ -809,7 +994,7 @@ struct Kern {
             *blocks_per_sm = known;
             return cudaSuccess;
         }
-        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP>;
+        auto kern = k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP, ROWS>;
         if (!attr[dev].load(std::memory_order_relaxed)) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem(NSTG == NSTAGE ? 16 : 1));
@@ -836,7 +1021,7 @@ struct Kern {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP>, a);
+        return cudaLaunchKernelEx(&cfg, k_gemv<MODE, NT, ABT, XSPLIT, NSTG, ONE, RBT, CMP, ROWS>, a);
     }
 };
 
@@ -847,25 +1032,31 @@ static cudaError_t dispatch_t(int path, int M, q4_dtype xt, bool deep, bool smal
         if constexpr (CMP) return cudaErrorInvalidValue;  // rejected before planning
         else return f(Kern<PATH_FMA, 1, 0, false>{});
     }
-    // small: 2-tile row blocks (2 <= M <= 8, 16-bit activations staged)
-    if (small && M >= 2 && M <= 8 && xt != Q4_F32) {
-        if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL, CMP>{});
-        return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL, CMP>{});
+    // 2 <= M <= 16, 16-bit activations: row-split consumers (4-tile row
+    // blocks for small problems)
+    if (M >= 2 && xt != Q4_F32) {
+        const bool two = M > 8;
+        if (small) {
+            if (xt == Q4_F16)
+                return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{})
+                           : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
+            return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{})
+                       : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
+        }
+        if (xt == Q4_F16)
+            return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB, CMP, true>{})
+                       : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB, CMP, true>{});
+        return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB, CMP, true>{})
+                   : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB, CMP, true>{});
     }
     // deep: M = 1, where a 3-stage ring still fits two CTAs per SM
     const bool two = M > 8;
-    if (xt == Q4_F16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 1, false, 3, true, RB, CMP>{});
-        if (M == 1) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, true, RB, CMP>{});
-        return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB, CMP>{})
-                   : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB, CMP>{});
-    }
-    if (xt == Q4_BF16) {
-        if (deep) return f(Kern<PATH_MMA, 1, 0, false, 3, true, RB, CMP>{});
-        if (M == 1) return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true, RB, CMP>{});
-        return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB, CMP>{})
-                   : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB, CMP>{});
-    }
+    if (xt == Q4_F16)  // M == 1
+        return deep ? f(Kern<PATH_MMA, 1, 1, false, 3, true, RB, CMP>{})
+                    : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, true, RB, CMP>{});
+    if (xt == Q4_BF16)
+        return deep ? f(Kern<PATH_MMA, 1, 0, false, 3, true, RB, CMP>{})
+                    : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, true, RB, CMP>{});
     if (M == 1)
         return deep ? f(Kern<PATH_MMA, 1, 0, true, 3, true, RB, CMP>{})
                     : f(Kern<PATH_MMA, 1, 0, true, NSTAGE, true, RB, CMP>{});
@@ -947,16 +1138,16 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     cudaGetDevice(&dev);
     cudaError_t cfg = dispatch(cmp, path, M, xt, false, false,
                                [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
-    // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 8: use
-    // 2-tile ones, so that steps are short and plentiful (measured faster
-    // there; at M = 1 the longer steps win).
+    // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 16: use
+    // 4-tile ones (one row tile per consumer warp), so that steps are short
+    // and plentiful (at M = 1 the longer steps win).
     const int64_t T8 = static_cast<int64_t>((ntiles + RB - 1) / RB) * NS;
     p.small = T8 < 4 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 2 &&
-              M <= 8 && xt != Q4_F32;
+              xt != Q4_F32;
     if (p.small && cfg == cudaSuccess)
         cfg = dispatch(cmp, path, M, xt, false, true,
                        [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
-    p.rb = p.small ? RB_SMALL : RB;
+    p.rb = p.small ? RB_SMALL_ROWS : RB;
     p.nrb = (ntiles + p.rb - 1) / p.rb;
     const int64_t T = static_cast<int64_t>(p.nrb) * NS;
     const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
