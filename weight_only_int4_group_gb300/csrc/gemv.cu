@@ -542,8 +542,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
         grid_dep_wait();
         if (beg < end) {
             constexpr int R16 = RB * 16;
-            const int Mo = (MODE == PATH_FMA || ONE) ? 1 : a.M;
+            // one batch row (compile time): scalar partial sums, as measured
+            // fastest there; otherwise 16-byte accesses
+            constexpr bool M1 = MODE == PATH_FMA || ONE;
+            const int Mo = M1 ? 1 : a.M;
             const int64_t slab4 = static_cast<int64_t>(R16 / 4) * Mo;  // one partial, in float4
+            const int64_t slab = static_cast<int64_t>(R16) * Mo;
             const int rb_first = static_cast<int>(beg / NS), rb_last = static_cast<int>((end - 1) / NS);
             for (int rb = rb_first, e = 0; rb <= rb_last; ++rb, ++e) {
                 const bool ok = mbar_wait_bounded(ofull, e & 1, abort_flag, a.wait_ns, a.err);
@@ -553,12 +557,66 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 const int c_last = static_cast<int>(owner_of(first_item + NS - 1, T, Gc));
                 const int nc = c_last - c_first + 1;
                 const int row0 = rb * R16;
+                const int nout = min(RB, ntiles - rb * RB) * 16 * Mo;
                 const int nval = min(min(RB, ntiles - rb * RB) * 16, a.N - row0);  // rows that exist
                 if (nc == 1) {
-                    for (int i = lane; i < Mo * R16; i += 32) {
-                        const int m = i / R16, row = i % R16;
-                        if (row < nval)
-                            store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
+                    if constexpr (M1) {
+                        for (int i = lane; i < nout; i += 32)
+                            if (row0 + i < a.N) store_y(a.y, a.yt, row0 + i, out[i]);
+                    } else {
+                        for (int i = lane; i < Mo * R16; i += 32) {
+                            const int m = i / R16, row = i % R16;
+                            if (row < nval)
+                                store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
+                        }
+                    }
+                } else if constexpr (M1) {
+                    float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
+                    for (int i = lane; i < nout; i += 32)
+                        part[(blockIdx.x - c_first) * slab + i] = out[i];
+                    __syncwarp();
+                    unsigned int prev = 0;
+                    if (lane == 0) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    __syncwarp();
+                    if (prev == static_cast<unsigned int>(nc - 1)) {
+                        // last to arrive: every partial is visible.  Four
+                        // outputs x four contributors of loads in flight at
+                        // once; the sums still run in CTA order.
+                        for (int i0 = lane; i0 < nout; i0 += 4 * 32) {
+                            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            for (int c0 = 0; c0 < nc; c0 += 4) {
+                                float pv[4][4];
+#pragma unroll
+                                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int i = i0 + 32 * u;
+                                        pv[cc][u] = (c0 + cc < nc && i < nout)
+                                                        ? __ldcg(&part[(c0 + cc) * slab + i])
+                                                        : 0.0f;
+                                    }
+#pragma unroll
+                                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u)
+                                        if (c0 + cc < nc) {
+                                            v[u] += pv[cc][u];
+                                            // consumed: the workspace goes back to zero
+                                            if (i0 + 32 * u < nout)
+                                                part[(c0 + cc) * slab + i0 + 32 * u] = 0.0f;
+                                        }
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = i0 + 32 * u;
+                                if (i >= nout) continue;
+                                const int row = i / Mo, m = i % Mo;
+                                if (row0 + row < a.N)
+                                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v[u]);
+                            }
+                        }
+                        if (lane == 0) a.count[rb] = 0u;  // ready for the next call
                     }
                 } else {
                     float4 *part = reinterpret_cast<float4 *>(a.partial) + (static_cast<int64_t>(rb) * a.maxc) * slab4;
@@ -948,7 +1006,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
             ok = false;
             break;
         }
-        {
+        if constexpr (MODE == PATH_FMA || ONE) {  // one batch row: [rows]
+            for (int i = threadIdx.x; i < nrt * 16; i += CONSUMERS) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) v += red[w * RB * 16 + i];
+                out[i] = v;
+            }
+        } else {
             const int nrows = nrt * 16;
             for (int i = threadIdx.x; i < nrows * Mo; i += CONSUMERS) {
                 const int m = i / nrows, row = i % nrows;
