@@ -298,7 +298,6 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
             ++rb;
         }
         const int slot = gstep % NSTG;
-        const int nrt = min(RB, ntiles - rb * RB);
         if (it == beg || s == 0) {
 #pragma unroll
             for (int r = 0; r < TPW; ++r)
@@ -322,38 +321,42 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
                 for (int jj = 0; jj < 4; ++jj)
                     ldmatrix_x4(bf[n][2 * jj][0], bf[n][2 * jj][1], bf[n][2 * jj + 1][0],
                                 bf[n][2 * jj + 1][1], xs + xoff[n] + gi * G * 2 + jj * 64);
-            // group sums of the activations (all-ones A), one MMA per k-step
-            float S[NT][4];
+            // this warp's row tiles of the group: codes and metadata.  Tiles
+            // past the matrix (last row block) hold stale stage bytes; their
+            // rows are computed but never written out.
+            uint32_t wv[TPW][8];
+            float2 sp[TPW];
+            uint32_t zp[TPW];
+#pragma unroll
+            for (int r = 0; r < TPW; ++r) {
+                const uint8_t *tile = stage + ((warp * TPW + r) * W + gi) * TBY;
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
+                tile_meta<CMP>(tile, gq, sp[r], zp[r]);
+                wv[r][0] = c0.x; wv[r][1] = c0.y; wv[r][2] = c0.z; wv[r][3] = c0.w;
+                wv[r][4] = c1.x; wv[r][5] = c1.y; wv[r][6] = c1.z; wv[r][7] = c1.w;
+            }
+            // k-step outer, tiles inner: TPW * NT independent accumulator
+            // chains plus NT for the group sums (all-ones A)
+            float S[NT][4], d[TPW][NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) S[n][e] = 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    S[n][e] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+                    for (int r = 0; r < TPW; ++r) d[r][n][e] = 0.0f;
+                }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
                     mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, bf[n][j][0], bf[n][j][1]);
 #pragma unroll
-            for (int r = 0; r < TPW; ++r) {
-                const int tr = warp * TPW + r;
-                if (tr >= nrt) break;  // warp-uniform: tiles past the matrix
-                const uint8_t *tile = stage + (tr * W + gi) * TBY;
-                const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
-                const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
-                float2 sp;
-                uint32_t zp;
-                tile_meta<CMP>(tile, gq, sp, zp);
-                const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                float d[NT][4];
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) d[n][e] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t w = wv[j];
+                for (int r = 0; r < TPW; ++r) {
+                    const uint32_t w = wv[r][j];
                     if (NT == 1) {
-                        mma_word<ABT>(d[0], w, bf[0][j][0], bf[0][j][1]);
+                        mma_word<ABT>(d[r][0], w, bf[0][j][0], bf[0][j][1]);
                     } else {
                         const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
                         const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
@@ -361,19 +364,22 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
                         const uint32_t a2 = lop3_and_or(w >> 12, 0x000F000Fu, MAG);
 #pragma unroll
                         for (int n = 0; n < NT; ++n)
-                            mma_ab<ABT>(d[n], a0, a1, a2, a3, bf[n][j][0], bf[n][j][1]);
+                            mma_ab<ABT>(d[r][n], a0, a1, a2, a3, bf[n][j][0], bf[n][j][1]);
                     }
                 }
+            }
+#pragma unroll
+            for (int r = 0; r < TPW; ++r) {
                 // OFF + zero: the byte under the exponent of 2^23
-                const float zg = __uint_as_float(__byte_perm(zp, 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
-                const float zg8 = __uint_as_float(__byte_perm(zp, 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
+                const float zg = __uint_as_float(__byte_perm(zp[r], 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
+                const float zg8 = __uint_as_float(__byte_perm(zp[r], 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     float *ya = yacc[r][n];
-                    ya[0] = fmaf(sp.x, fmaf(-zg, S[n][0], d[n][0]), ya[0]);
-                    ya[1] = fmaf(sp.x, fmaf(-zg, S[n][1], d[n][1]), ya[1]);
-                    ya[2] = fmaf(sp.y, fmaf(-zg8, S[n][0], d[n][2]), ya[2]);
-                    ya[3] = fmaf(sp.y, fmaf(-zg8, S[n][1], d[n][3]), ya[3]);
+                    ya[0] = fmaf(sp[r].x, fmaf(-zg, S[n][0], d[r][n][0]), ya[0]);
+                    ya[1] = fmaf(sp[r].x, fmaf(-zg, S[n][1], d[r][n][1]), ya[1]);
+                    ya[2] = fmaf(sp[r].y, fmaf(-zg8, S[n][0], d[r][n][2]), ya[2]);
+                    ya[3] = fmaf(sp[r].y, fmaf(-zg8, S[n][1], d[r][n][3]), ya[3]);
                 }
             }
         }
