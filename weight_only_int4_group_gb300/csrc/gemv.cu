@@ -310,76 +310,111 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
         if (!__all_sync(0xffffffffu, ok)) return;
         const uint8_t *stage = ring + slot * SB;
         const uint8_t *xs = stage + TILES_BYTES;
+        // GP groups at a time (two at once measured slower at one batch tile,
+        // and two batch tiles have no registers to spare)
+        constexpr int GP = 1;
 #pragma unroll 1
-        for (int gi = 0; gi < W; ++gi) {
-            if (s * W + gi >= NG) break;  // the last step may hold fewer groups
-            // B fragments of the group's 8 k-steps for every batch tile
-            uint32_t bf[NT][8][2];
+        for (int gi0 = 0; gi0 < W; gi0 += GP) {
+            if (s * W + gi0 >= NG) break;  // the last step may hold fewer groups
+            // B fragments of the groups' 8 k-steps for every batch tile; a
+            // group past K (odd group count) reads the stage's bytes and is
+            // discarded
+            uint32_t bf[GP][NT][8][2];
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
+            for (int gp = 0; gp < GP; ++gp)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    ldmatrix_x4(bf[n][2 * jj][0], bf[n][2 * jj][1], bf[n][2 * jj + 1][0],
-                                bf[n][2 * jj + 1][1], xs + xoff[n] + gi * G * 2 + jj * 64);
-            // this warp's row tiles of the group: codes and metadata.  Tiles
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        ldmatrix_x4(bf[gp][n][2 * jj][0], bf[gp][n][2 * jj][1], bf[gp][n][2 * jj + 1][0],
+                                    bf[gp][n][2 * jj + 1][1], xs + xoff[n] + (gi0 + gp) * G * 2 + jj * 64);
+            // this warp's row tiles of the groups: codes and metadata.  Tiles
             // past the matrix (last row block) hold stale stage bytes; their
             // rows are computed but never written out.
-            uint32_t wv[TPW][8];
-            float2 sp[TPW];
-            uint32_t zp[TPW];
+            uint32_t wv[GP][TPW][8];
+            float2 sp[GP][TPW];
+            uint32_t zp[GP][TPW];
 #pragma unroll
-            for (int r = 0; r < TPW; ++r) {
-                const uint8_t *tile = stage + ((warp * TPW + r) * W + gi) * TBY;
-                const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
-                const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
-                tile_meta<CMP>(tile, gq, sp[r], zp[r]);
-                wv[r][0] = c0.x; wv[r][1] = c0.y; wv[r][2] = c0.z; wv[r][3] = c0.w;
-                wv[r][4] = c1.x; wv[r][5] = c1.y; wv[r][6] = c1.z; wv[r][7] = c1.w;
-            }
-            // k-step outer, tiles inner: TPW * NT independent accumulator
-            // chains plus NT for the group sums (all-ones A)
-            float S[NT][4], d[TPW][NT][4];
+            for (int gp = 0; gp < GP; ++gp)
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    S[n][e] = 0.0f;
-#pragma unroll
-                    for (int r = 0; r < TPW; ++r) d[r][n][e] = 0.0f;
+                for (int r = 0; r < TPW; ++r) {
+                    const uint8_t *tile = stage + ((warp * TPW + r) * W + gi0 + gp) * TBY;
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
+                    tile_meta<CMP>(tile, gq, sp[gp][r], zp[gp][r]);
+                    wv[gp][r][0] = c0.x; wv[gp][r][1] = c0.y; wv[gp][r][2] = c0.z; wv[gp][r][3] = c0.w;
+                    wv[gp][r][4] = c1.x; wv[gp][r][5] = c1.y; wv[gp][r][6] = c1.z; wv[gp][r][7] = c1.w;
                 }
+            // k-step outer, groups and tiles inner: GP * TPW * NT independent
+            // accumulator chains plus the group sums.  One batch tile: an
+            // all-ones A times the activations gives lane (g, t) the sums of
+            // batch rows 2t, 2t + 1.  Two batch tiles: the 16 activation rows
+            // as A times all-ones B give lane (g, t) the sums of rows g and
+            // g + 8 (one MMA instead of two), redistributed by shuffles below.
+            float S[GP][NT][4], d[GP][TPW][NT][4];
+#pragma unroll
+            for (int gp = 0; gp < GP; ++gp)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        S[gp][n][e] = 0.0f;
+#pragma unroll
+                        for (int r = 0; r < TPW; ++r) d[gp][r][n][e] = 0.0f;
+                    }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
-                    mma_ab<ABT>(S[n], ONES, ONES, ONES, ONES, bf[n][j][0], bf[n][j][1]);
+                for (int gp = 0; gp < GP; ++gp) {
+                    if (NT == 1)
+                        mma_ab<ABT>(S[gp][0], ONES, ONES, ONES, ONES, bf[gp][0][j][0], bf[gp][0][j][1]);
+                    else
+                        mma_ab<ABT>(S[gp][0], bf[gp][0][j][0], bf[gp][NT - 1][j][0], bf[gp][0][j][1],
+                                    bf[gp][NT - 1][j][1], ONES, ONES);
 #pragma unroll
-                for (int r = 0; r < TPW; ++r) {
-                    const uint32_t w = wv[r][j];
-                    if (NT == 1) {
-                        mma_word<ABT>(d[r][0], w, bf[0][j][0], bf[0][j][1]);
-                    } else {
-                        const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
-                        const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
-                        const uint32_t a3 = lop3_and_or(w >> 8, 0x000F000Fu, MAG);
-                        const uint32_t a2 = lop3_and_or(w >> 12, 0x000F000Fu, MAG);
+                    for (int r = 0; r < TPW; ++r) {
+                        const uint32_t w = wv[gp][r][j];
+                        if (NT == 1) {
+                            mma_word<ABT>(d[gp][r][0], w, bf[gp][0][j][0], bf[gp][0][j][1]);
+                        } else {
+                            const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
+                            const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
+                            const uint32_t a3 = lop3_and_or(w >> 8, 0x000F000Fu, MAG);
+                            const uint32_t a2 = lop3_and_or(w >> 12, 0x000F000Fu, MAG);
 #pragma unroll
-                        for (int n = 0; n < NT; ++n)
-                            mma_ab<ABT>(d[r][n], a0, a1, a2, a3, bf[n][j][0], bf[n][j][1]);
+                            for (int n = 0; n < NT; ++n)
+                                mma_ab<ABT>(d[gp][r][n], a0, a1, a2, a3, bf[gp][n][j][0], bf[gp][n][j][1]);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int r = 0; r < TPW; ++r) {
-                // OFF + zero: the byte under the exponent of 2^23
-                const float zg = __uint_as_float(__byte_perm(zp[r], 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
-                const float zg8 = __uint_as_float(__byte_perm(zp[r], 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
+            for (int gp = 0; gp < GP; ++gp) {
+                if (s * W + gi0 + gp >= NG) break;  // past K: nothing to add
+                float Sc[NT][2];  // sums of batch rows 8n + 2t and 8n + 2t + 1
+                if (NT == 1) {
+                    Sc[0][0] = S[gp][0][0];
+                    Sc[0][1] = S[gp][0][1];
+                } else {
+                    // S[gp][0][0] = sum of row g, S[gp][0][2] = sum of row g + 8
+                    Sc[0][0] = __shfl_sync(0xffffffffu, S[gp][0][0], 8 * t);
+                    Sc[0][1] = __shfl_sync(0xffffffffu, S[gp][0][0], 8 * t + 4);
+                    Sc[NT - 1][0] = __shfl_sync(0xffffffffu, S[gp][0][2], 8 * t);
+                    Sc[NT - 1][1] = __shfl_sync(0xffffffffu, S[gp][0][2], 8 * t + 4);
+                }
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    float *ya = yacc[r][n];
-                    ya[0] = fmaf(sp[r].x, fmaf(-zg, S[n][0], d[r][n][0]), ya[0]);
-                    ya[1] = fmaf(sp[r].x, fmaf(-zg, S[n][1], d[r][n][1]), ya[1]);
-                    ya[2] = fmaf(sp[r].y, fmaf(-zg8, S[n][0], d[r][n][2]), ya[2]);
-                    ya[3] = fmaf(sp[r].y, fmaf(-zg8, S[n][1], d[r][n][3]), ya[3]);
+                for (int r = 0; r < TPW; ++r) {
+                    // OFF + zero: the byte under the exponent of 2^23
+                    const float zg = __uint_as_float(__byte_perm(zp[gp][r], 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
+                    const float zg8 = __uint_as_float(__byte_perm(zp[gp][r], 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        float *ya = yacc[r][n];
+                        ya[0] = fmaf(sp[gp][r].x, fmaf(-zg, Sc[n][0], d[gp][r][n][0]), ya[0]);
+                        ya[1] = fmaf(sp[gp][r].x, fmaf(-zg, Sc[n][1], d[gp][r][n][1]), ya[1]);
+                        ya[2] = fmaf(sp[gp][r].y, fmaf(-zg8, Sc[n][0], d[gp][r][n][2]), ya[2]);
+                        ya[3] = fmaf(sp[gp][r].y, fmaf(-zg8, Sc[n][1], d[gp][r][n][3]), ya[3]);
+                    }
                 }
             }
         }
@@ -539,8 +574,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
     // is written out directly.  Otherwise the partial sums go to this CTA's
     // slot of the workspace (16-byte copies) and the arrival counter is
     // stepped; the contributor that arrives last sums the partials of all
-    // contributors in CTA order (the same order whoever arrives last; four
-    // 16-byte loads per contributor in flight per lane), and clears the
+    // contributors in CTA order (the same order whoever arrives last; up to
+    // eight 16-byte loads per contributor in flight per lane), and clears the
     // partials it read and the counter, so a completed call leaves the
     // workspace zero for the next one, whatever its shape.
     if (warp == W + 1) {
@@ -635,26 +670,31 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                     prev = __shfl_sync(0xffffffffu, prev, 0);
                     __syncwarp();
                     if (prev == static_cast<unsigned int>(nc - 1)) {
-                        // last to arrive: every partial is visible
-                        for (int i0 = lane; i0 < slab4; i0 += 4 * 32) {
-                            float4 v[4];
+                        // last to arrive: every partial is visible.  U
+                        // 16-byte loads per lane for each of two contributors
+                        // in flight at once (8 for the larger partials of two
+                        // batch tiles; 4 measured faster below); the sums run
+                        // in CTA order.
+                        constexpr int U = NT == 2 ? 8 : 4;
+                        for (int i0 = lane; i0 < slab4; i0 += U * 32) {
+                            float4 v[U];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int c0 = 0; c0 < nc; c0 += 4) {
-                                float4 pv[4][4];
+                            for (int u = 0; u < U; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int c0 = 0; c0 < nc; c0 += 2) {
+                                float4 pv[2][U];
 #pragma unroll
-                                for (int cc = 0; cc < 4; ++cc)
+                                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
+                                    for (int u = 0; u < U; ++u) {
                                         const int64_t i = i0 + 32 * u;
                                         pv[cc][u] = (c0 + cc < nc && i < slab4)
                                                         ? __ldcg(&part[(c0 + cc) * slab4 + i])
                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                                     }
 #pragma unroll
-                                for (int cc = 0; cc < 4; ++cc)
+                                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
+                                    for (int u = 0; u < U; ++u) {
                                         const int64_t i = i0 + 32 * u;
                                         if (c0 + cc < nc && i < slab4) {
                                             v[u].x += pv[cc][u].x;
@@ -667,7 +707,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                     }
                             }
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
+                            for (int u = 0; u < U; ++u) {
                                 const int i = i0 + 32 * u;
                                 if (i >= slab4) continue;
                                 const int m = (4 * i) / R16, row = (4 * i) % R16;
