@@ -66,7 +66,8 @@ typedef enum {
     Q4_ERR_UNSUPPORTED = 2,
     Q4_ERR_MISALIGNED = 3,
     Q4_ERR_CUDA = 4,
-    Q4_ERR_TIMEOUT = 5
+    Q4_ERR_TIMEOUT = 5,
+    Q4_ERR_BOUNDS = 6
 } q4_status;
 
 typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
@@ -309,13 +310,26 @@ q4_status q4_gemv_noalloc(const void *x, q4_dtype xt, int64_t M, int64_t N, int6
                           q4_dtype yt, q4_stream_t stream);
 
 /* Synchronises `stream` and reports errors raised on the device since the
- * last check: Q4_ERR_TIMEOUT when a bounded wait inside a kernel gave up
- * (the kernel then returned without writing its outputs), Q4_ERR_CUDA for a
- * CUDA error, else Q4_OK.  Clears the device error word. */
+ * last check: Q4_ERR_BOUNDS when, in a library built with -DQ4_DEBUG, a
+ * kernel computed a global store outside the buffer it writes (the store was
+ * skipped; release builds do not check), Q4_ERR_TIMEOUT when a bounded wait
+ * inside a kernel gave up (the kernel then returned without writing its
+ * outputs), Q4_ERR_CUDA for a CUDA error, else Q4_OK.  Clears the device
+ * error word. */
 q4_status q4_check(q4_stream_t stream);
 
 /* Static description of a status code. */
 const char *q4_status_str(q4_status status);
+
+/* Self-test of the store checks of a -DQ4_DEBUG build.  `buf`: at least 32
+ * bytes of device memory.  One kernel writes byte i = i + 1 for i in 0..31
+ * through the same check the other kernels use, declaring an extent of 16
+ * bytes: bytes 0..15 are written, bytes 16..31 are left as they were and the
+ * device error word records the skipped stores (the next q4_check returns
+ * Q4_ERR_BOUNDS).  Every store the kernel attempts lies inside the 32 bytes,
+ * so the test is safe even if the check were wrong.  A release build returns
+ * Q4_ERR_UNSUPPORTED and launches nothing. */
+q4_status q4_debug_bounds_selftest(uint8_t *buf, q4_stream_t stream);
 
 /* Text of the most recent CUDA error seen by this library in this thread. */
 const char *q4_last_cuda_error(void);

@@ -28,3 +28,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _no_store_outside_buffers(request):
+    """Against a bounds-checked library build (Q4_LIBRARY set), every GPU
+    test ends with a q4_check that must not report a store outside its
+    buffer."""
+    yield
+    if not os.environ.get("Q4_LIBRARY") or "gpu" not in request.node.keywords:
+        return
+    import weight_only_int4_group_gb300 as q4
+    assert q4.check() != q4.ERR_BOUNDS, "a kernel store fell outside its buffer"

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
                  "q4_unpack_compact", "q4_xsum", "q4_gemv", "q4_gemv_path", "q4_gemm",
                  "q4_check", "q4_status_str", "q4_weight_bytes", "q4_gemv_workspace_bytes",
                  "q4_gemm_workspace_bytes", "q4_gemv_timeout_selftest", "q4_gemm_timeout_selftest",
-                 "q4_gemv_noalloc"):
+                 "q4_gemv_noalloc", "q4_debug_bounds_selftest"):
         assert must in names
 
 
@@ -48,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     lib.q4_status_str.restype = ctypes.c_char_p
-    for s in range(6):
+    for s in range(7):
         assert lib.q4_status_str(s)
     assert b"unknown" in lib.q4_status_str(99)
 

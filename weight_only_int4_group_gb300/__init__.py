@@ -21,14 +21,16 @@ from dataclasses import dataclass
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libq4.so")
+# Q4_LIBRARY selects another build of the same library (the bounds-checked
+# libq4_debug.so); the named file must exist, there is no fallback.
+LIB_PATH = os.environ.get("Q4_LIBRARY") or os.path.join(_HERE, "libq4.so")
 GROUP = 128
 TILE_ROWS = 16
 TILE_BYTES = 1104
 CMP_TILE_BYTES = 1072
 GEMV_MAX_M = 16
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = range(7)
 F32, BF16, F16 = 0, 1, 2
 LAYOUT_TILED, LAYOUT_COMPACT = 1, 2
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
@@ -72,12 +74,14 @@ def _load():
     lib.q4_gemm_timeout_selftest.argtypes = prod
     lib.q4_gemv_noalloc.argtypes = [P, S, I, I, I, P, S, Z, P, S, P]
     lib.q4_check.argtypes = [P]
+    lib.q4_debug_bounds_selftest.argtypes = [P, P]
     lib.q4_status_str.argtypes = [S]
     lib.q4_status_str.restype = ctypes.c_char_p
     lib.q4_last_cuda_error.restype = ctypes.c_char_p
     for f in ("q4_quantize", "q4_quantize_sym", "q4_repack", "q4_unpack", "q4_repack_compact",
               "q4_unpack_compact", "q4_xsum", "q4_gemv", "q4_gemv_path", "q4_gemv_timeout_selftest",
-              "q4_gemm", "q4_gemm_timeout_selftest", "q4_gemv_noalloc", "q4_check"):
+              "q4_gemm", "q4_gemm_timeout_selftest", "q4_gemv_noalloc", "q4_check",
+              "q4_debug_bounds_selftest"):
         getattr(lib, f).restype = S
     return lib
 

@@ -58,6 +58,18 @@ unsigned int *device_error_word()
     return d ? d->err : nullptr;
 }
 
+// The error word for the store checks of the packing kernels: looked up
+// only in debug builds, so release calls stay free of the device query.
+static inline unsigned int *debug_err() { return kDebugBounds ? device_error_word() : nullptr; }
+
+// Stores i + 1 into byte i of a 32-byte buffer through the store check,
+// declaring an extent of 16.
+__global__ void k_bounds_selftest(uint8_t *buf, unsigned int *err)
+{
+    const int i = threadIdx.x;
+    if (i < 32 && store_ok(i, 16, err)) buf[i] = static_cast<uint8_t>(i + 1);
+}
+
 static inline bool sizes_ok(int64_t N, int64_t K)
 {
     return N >= 1 && K >= G && K % G == 0 && N <= (1LL << 30) && K <= (1LL << 30) &&
@@ -111,9 +123,12 @@ static q4_status gemv_common(const void *x, q4_dtype xt, int64_t M, int64_t N, i
     a.yt = yt;
     a.maxc = plan.maxc;
     if (plan.maxc > 1) {
+        const size_t counters = gemv_counter_bytes(N);
         a.count = static_cast<unsigned int *>(workspace);
-        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                              gemv_counter_bytes(N));
+        a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters);
+        // store checks use the plan's own extents (inside the caller's buffer)
+        a.count_len = plan.nrb;
+        a.partial_len = static_cast<int64_t>((plan.workspace - counters) / sizeof(float));
     }
     a.wait_ns = wait_ns;
     a.err = d->err;
@@ -133,7 +148,7 @@ static q4_status quantize_common(const float *w, int64_t N, int64_t K, uint8_t *
 {
     if (!w || !packed || !scale || !zero || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(w)) return Q4_ERR_MISALIGNED;
-    const cudaError_t e = quantize_launch(w, N, K, packed, scale, zero, symmetric,
+    const cudaError_t e = quantize_launch(w, N, K, packed, scale, zero, symmetric, debug_err(),
                                           reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
@@ -161,7 +176,7 @@ q4_status q4_repack(const uint8_t *packed, const float *scale, const uint8_t *ze
     if (!packed || !scale || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
     const cudaError_t e = repack_launch(packed, scale, zero, N, K, static_cast<uint8_t *>(qw),
-                                        reinterpret_cast<cudaStream_t>(stream));
+                                        debug_err(), reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
 
@@ -171,7 +186,7 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
     if (!packed || !scale || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
     const cudaError_t e = unpack_launch(static_cast<const uint8_t *>(qw), N, K, packed, scale,
-                                        zero, reinterpret_cast<cudaStream_t>(stream));
+                                        zero, debug_err(), reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
 
@@ -181,7 +196,7 @@ q4_status q4_repack_compact(const uint8_t *packed, const float *scale, const uin
     if (!packed || !scale || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
     const cudaError_t e = repack_compact_launch(packed, scale, zero, N, K,
-                                                static_cast<uint8_t *>(qw),
+                                                static_cast<uint8_t *>(qw), debug_err(),
                                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
@@ -192,7 +207,7 @@ q4_status q4_unpack_compact(const void *qw, int64_t N, int64_t K, uint8_t *packe
     if (!packed || !scale16 || !zero || !qw || !sizes_ok(N, K)) return Q4_ERR_INVALID_ARG;
     if (!aligned16(qw)) return Q4_ERR_MISALIGNED;
     const cudaError_t e = unpack_compact_launch(static_cast<const uint8_t *>(qw), N, K, packed,
-                                                scale16, zero,
+                                                scale16, zero, debug_err(),
                                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
@@ -202,7 +217,8 @@ q4_status q4_xsum(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
 {
     if (!x || !xsum || M < 1 || !sizes_ok(M, K)) return Q4_ERR_INVALID_ARG;
     if (!valid_dtype(xt)) return Q4_ERR_UNSUPPORTED;
-    const cudaError_t e = xsum_launch(x, xt, M, K, xsum, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = xsum_launch(x, xt, M, K, xsum, debug_err(),
+                                      reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q4_OK : cuda_fail(e);
 }
 
@@ -313,7 +329,7 @@ q4_status q4_check(q4_stream_t stream)
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(g_q4_error, &zero, sizeof(zero));
         if (e != cudaSuccess) return cuda_fail(e);
-        return Q4_ERR_TIMEOUT;
+        return (word & ERR_BOUNDS) ? Q4_ERR_BOUNDS : Q4_ERR_TIMEOUT;
     }
     return Q4_OK;
 }
@@ -327,10 +343,22 @@ const char *q4_status_str(q4_status status)
     case Q4_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case Q4_ERR_CUDA: return "CUDA error";
     case Q4_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case Q4_ERR_BOUNDS: return "a store outside its buffer was skipped (debug build)";
     }
     return "unknown status";
 }
 
 const char *q4_last_cuda_error(void) { return t_last_error; }
+
+q4_status q4_debug_bounds_selftest(uint8_t *buf, q4_stream_t stream)
+{
+    if (!kDebugBounds) return Q4_ERR_UNSUPPORTED;
+    if (!buf) return Q4_ERR_INVALID_ARG;
+    const DevInfo *d = dev_info();
+    if (!d) return cuda_fail(cudaGetLastError());
+    k_bounds_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(buf, d->err);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4_OK : cuda_fail(e);
+}
 
 }  // extern "C"

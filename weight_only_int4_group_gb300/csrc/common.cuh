@@ -34,7 +34,26 @@ constexpr int CMP_ZERO_OFF = 1056;
 // every kernel that waits): bit 0 = a bounded wait timed out.  Read and
 // cleared by q4_check.
 constexpr unsigned int ERR_TIMEOUT = 1u;
+constexpr unsigned int ERR_BOUNDS = 2u;  // a store outside its buffer (Q4_DEBUG builds)
 unsigned int *device_error_word();  // host: address on the current device
+
+#ifdef Q4_DEBUG
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+// Debug builds (-DQ4_DEBUG) check every global store of the kernels against
+// the extent of its buffer: an index outside [0, limit) raises ERR_BOUNDS in
+// the device error word and the caller skips the store (no trap, no fault;
+// q4_check reports Q4_ERR_BOUNDS).  Release builds compile the check away.
+__device__ __forceinline__ bool store_ok(int64_t idx, int64_t limit, unsigned int *err)
+{
+    if constexpr (!kDebugBounds) return true;
+    if (idx >= 0 && idx < limit) return true;
+    if (err) atomicOr(err, ERR_BOUNDS);
+    return false;
+}
 
 // Host: keeps the CUDA error's text for q4_last_cuda_error (this thread) and
 // returns Q4_ERR_CUDA.
@@ -226,6 +245,8 @@ struct GemvArgs {
     q4_dtype yt;
     float *partial;       // [nrb][maxc][64 rows][M] partial sums of shared row blocks
     unsigned int *count;  // [nrb] arrival counters of shared row blocks
+    int64_t partial_len;  // floats the workspace holds at `partial` (store checks)
+    int64_t count_len;    // counters the workspace holds at `count` (store checks)
     int maxc;             // most CTAs that share one row block
     uint64_t wait_ns;     // bound of every mbarrier wait
     unsigned int *err;    // device error word
@@ -253,15 +274,17 @@ size_t gemv_counter_bytes(int64_t N);
 cudaError_t gemv_launch(const GemvPlan &plan, const GemvArgs &a, cudaStream_t s);
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                            uint8_t *zero, bool symmetric, cudaStream_t s);
+                            uint8_t *zero, bool symmetric, unsigned int *err, cudaStream_t s);
 cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
-                          int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
+                          int64_t N, int64_t K, uint8_t *qw, unsigned int *err, cudaStream_t s);
 cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                          uint8_t *zero, cudaStream_t s);
+                          uint8_t *zero, unsigned int *err, cudaStream_t s);
 cudaError_t repack_compact_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
-                                  int64_t N, int64_t K, uint8_t *qw, cudaStream_t s);
+                                  int64_t N, int64_t K, uint8_t *qw, unsigned int *err,
+                                  cudaStream_t s);
 cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed,
-                                  uint16_t *scale16, uint8_t *zero, cudaStream_t s);
+                                  uint16_t *scale16, uint8_t *zero, unsigned int *err,
+                                  cudaStream_t s);
 // Large-M GEMM plan: tiles of 128 weight rows x bt tokens; either every
 // tile is computed by one CTA (split == false, tiles dealt round robin) or
 // the tiles' groups form one sequence of items cut into equal contiguous
@@ -280,6 +303,6 @@ q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int
                    unsigned int *err, uint64_t wait_ns, int debug_no_copy, cudaStream_t s,
                    cudaError_t *cerr);
 cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
-                        cudaStream_t s);
+                        unsigned int *err, cudaStream_t s);
 
 }  // namespace q4

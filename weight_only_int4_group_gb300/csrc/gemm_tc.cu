@@ -231,6 +231,8 @@ struct Args {
     int maxc;              // most CTAs sharing one tile
     unsigned int *count;   // [tiles] arrival counters (split)
     float *partial;        // [tiles][maxc][128 rows][bt] partial sums (split)
+    int64_t count_len;     // extents of the two, for the store checks of debug builds
+    int64_t partial_len;
     uint64_t wait_ns;
     unsigned int *err;
     int debug_no_copy;     // the weight producer copies nothing (bounded-wait self-test)
@@ -282,6 +284,21 @@ __device__ __forceinline__ void store_out(void *y, q4_dtype yt, int64_t idx, flo
         static_cast<__nv_bfloat16 *>(y)[idx] = __float2bfloat16_rn(v);
     else
         static_cast<__half *>(y)[idx] = __float2half_rn(v);
+}
+
+// The epilogue's global stores, each checked against its buffer in debug
+// builds (a store outside it is recorded and skipped).
+__device__ __forceinline__ void put_out(const Args &a, int64_t idx, float v)
+{
+    if (store_ok(idx, static_cast<int64_t>(a.M) * a.N, a.err)) store_out(a.y, a.yt, idx, v);
+}
+__device__ __forceinline__ void put_part4(const Args &a, float4 *p, float4 v)
+{
+    if (store_ok(reinterpret_cast<float *>(p) - a.partial + 3, a.partial_len, a.err)) *p = v;
+}
+__device__ __forceinline__ bool count_ok(const Args &a, int tile)
+{
+    return store_ok(tile, a.count_len, a.err);
 }
 
 // F16: activations (and the A operand) are f16, else bf16.  BT: tokens per
@@ -624,7 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < NCOL; ++j)
                         if (m0 + j < a.M)
-                            store_out(a.y, a.yt, static_cast<int64_t>(m0 + j) * a.N + n, Y[j]);
+                            put_out(a, static_cast<int64_t>(m0 + j) * a.N + n, Y[j]);
                 continue;
             }
             // Split tile: publish this CTA's partial, count the arrival; the
@@ -635,11 +652,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float4 *dst = reinterpret_cast<float4 *>(part + (blockIdx.x - c_first) * slab);
 #pragma unroll
                 for (int j = 0; j < NCOL / 4; ++j)
-                    dst[j] = make_float4(Y[4 * j], Y[4 * j + 1], Y[4 * j + 2], Y[4 * j + 3]);
+                    put_part4(a, dst + j, make_float4(Y[4 * j], Y[4 * j + 1], Y[4 * j + 2], Y[4 * j + 3]));
             }
             __threadfence();
             named_barrier_sync(1, 256);
-            if (w == 0 && lane == 0) *bcast = atomic_add_acq_rel_gpu(&a.count[tile], 1u);
+            if (w == 0 && lane == 0)
+                *bcast = count_ok(a, tile) ? atomic_add_acq_rel_gpu(&a.count[tile], 1u) : 0u;
             named_barrier_sync(1, 256);
             const unsigned int prev = *bcast;
             if (prev == static_cast<unsigned int>(nc - 1)) {
@@ -659,16 +677,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                             v[4 * j + 3] += p.w;
                         }
 #pragma unroll
-                        for (int j = 0; j < NCOL / 4; ++j) src[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int j = 0; j < NCOL / 4; ++j) put_part4(a, src + j, make_float4(0.f, 0.f, 0.f, 0.f));
                     }
                     if (n < a.N)
 #pragma unroll
                         for (int j = 0; j < NCOL; ++j)
                             if (m0 + j < a.M)
-                                store_out(a.y, a.yt, static_cast<int64_t>(m0 + j) * a.N + n,
-                                                 v[j]);
+                                put_out(a, static_cast<int64_t>(m0 + j) * a.N + n, v[j]);
                 }
-                if (w == 0 && lane == 0) a.count[tile] = 0u;  // ready for the next call
+                if (w == 0 && lane == 0 && count_ok(a, tile)) a.count[tile] = 0u;  // ready for the next call
             }
         }
     }
@@ -790,6 +807,8 @@ q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int
         const size_t counters = ((static_cast<size_t>(T) * sizeof(unsigned int) + 255) / 256) * 256;
         a.count = static_cast<unsigned int *>(workspace);
         a.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters);
+        a.count_len = T;
+        a.partial_len = static_cast<int64_t>((p.workspace - counters) / sizeof(float));
     }
     a.wait_ns = wait_ns;
     a.err = err;

@@ -126,6 +126,25 @@ __device__ __forceinline__ void store_y(void *y, q4_dtype yt, int64_t idx, float
         static_cast<__half *>(y)[idx] = __float2half_rn(v);
 }
 
+// The epilogue's global stores, each checked against its buffer in debug
+// builds (a store outside it is recorded and skipped).
+__device__ __forceinline__ void put_y(const GemvArgs &a, int64_t idx, float v)
+{
+    if (store_ok(idx, static_cast<int64_t>(a.M) * a.N, a.err)) store_y(a.y, a.yt, idx, v);
+}
+__device__ __forceinline__ void put_part(const GemvArgs &a, float *p, float v)
+{
+    if (store_ok(p - a.partial, a.partial_len, a.err)) *p = v;
+}
+__device__ __forceinline__ void put_part4(const GemvArgs &a, float4 *p, float4 v)
+{
+    if (store_ok(reinterpret_cast<float *>(p) - a.partial + 3, a.partial_len, a.err)) *p = v;
+}
+__device__ __forceinline__ bool count_ok(const GemvArgs &a, int rb)
+{
+    return store_ok(rb, a.count_len, a.err);
+}
+
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
 {
@@ -605,21 +624,21 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                 if (nc == 1) {
                     if constexpr (M1) {
                         for (int i = lane; i < nout; i += 32)
-                            if (row0 + i < a.N) store_y(a.y, a.yt, row0 + i, out[i]);
+                            if (row0 + i < a.N) put_y(a, row0 + i, out[i]);
                     } else {
                         for (int i = lane; i < Mo * R16; i += 32) {
                             const int m = i / R16, row = i % R16;
                             if (row < nval)
-                                store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
+                                put_y(a, static_cast<int64_t>(m) * a.N + row0 + row, out[i]);
                         }
                     }
                 } else if constexpr (M1) {
                     float *part = a.partial + (static_cast<int64_t>(rb) * a.maxc) * slab;
                     for (int i = lane; i < nout; i += 32)
-                        part[(blockIdx.x - c_first) * slab + i] = out[i];
+                        put_part(a, &part[(blockIdx.x - c_first) * slab + i], out[i]);
                     __syncwarp();
                     unsigned int prev = 0;
-                    if (lane == 0) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
+                    if (lane == 0 && count_ok(a, rb)) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
                     prev = __shfl_sync(0xffffffffu, prev, 0);
                     __syncwarp();
                     if (prev == static_cast<unsigned int>(nc - 1)) {
@@ -647,7 +666,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                             v[u] += pv[cc][u];
                                             // consumed: the workspace goes back to zero
                                             if (i0 + 32 * u < nout)
-                                                part[(c0 + cc) * slab + i0 + 32 * u] = 0.0f;
+                                                put_part(a, &part[(c0 + cc) * slab + i0 + 32 * u], 0.0f);
                                         }
                             }
 #pragma unroll
@@ -656,19 +675,19 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                 if (i >= nout) continue;
                                 const int row = i / Mo, m = i % Mo;
                                 if (row0 + row < a.N)
-                                    store_y(a.y, a.yt, static_cast<int64_t>(m) * a.N + row0 + row, v[u]);
+                                    put_y(a, static_cast<int64_t>(m) * a.N + row0 + row, v[u]);
                             }
                         }
-                        if (lane == 0) a.count[rb] = 0u;  // ready for the next call
+                        if (lane == 0 && count_ok(a, rb)) a.count[rb] = 0u;  // ready for the next call
                     }
                 } else {
                     float4 *part = reinterpret_cast<float4 *>(a.partial) + (static_cast<int64_t>(rb) * a.maxc) * slab4;
                     float4 *mine = part + (blockIdx.x - c_first) * slab4;
                     const float4 *o4 = reinterpret_cast<const float4 *>(out);
-                    for (int i = lane; i < slab4; i += 32) mine[i] = o4[i];
+                    for (int i = lane; i < slab4; i += 32) put_part4(a, &mine[i], o4[i]);
                     __syncwarp();
                     unsigned int prev = 0;
-                    if (lane == 0) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
+                    if (lane == 0 && count_ok(a, rb)) prev = atomic_add_acq_rel_gpu(&a.count[rb], 1u);
                     prev = __shfl_sync(0xffffffffu, prev, 0);
                     __syncwarp();
                     if (prev == static_cast<unsigned int>(nc - 1)) {
@@ -704,7 +723,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                             v[u].z += pv[cc][u].z;
                                             v[u].w += pv[cc][u].w;
                                             // consumed: the workspace goes back to zero
-                                            part[(c0 + cc) * slab4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                            put_part4(a, &part[(c0 + cc) * slab4 + i],
+                                                      make_float4(0.f, 0.f, 0.f, 0.f));
                                         }
                                     }
                             }
@@ -714,13 +734,13 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                 if (i >= slab4) continue;
                                 const int m = (4 * i) / R16, row = (4 * i) % R16;
                                 const int64_t yb = static_cast<int64_t>(m) * a.N + row0 + row;
-                                if (row < nval) store_y(a.y, a.yt, yb, v[u].x);
-                                if (row + 1 < nval) store_y(a.y, a.yt, yb + 1, v[u].y);
-                                if (row + 2 < nval) store_y(a.y, a.yt, yb + 2, v[u].z);
-                                if (row + 3 < nval) store_y(a.y, a.yt, yb + 3, v[u].w);
+                                if (row < nval) put_y(a, yb, v[u].x);
+                                if (row + 1 < nval) put_y(a, yb + 1, v[u].y);
+                                if (row + 2 < nval) put_y(a, yb + 2, v[u].z);
+                                if (row + 3 < nval) put_y(a, yb + 3, v[u].w);
                             }
                         }
-                        if (lane == 0) a.count[rb] = 0u;  // ready for the next call
+                        if (lane == 0 && count_ok(a, rb)) a.count[rb] = 0u;  // ready for the next call
                     }
                 }
                 __syncwarp();

@@ -95,7 +95,7 @@ template <bool SYM>
 __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, int64_t ngroups,
                                                   uint8_t *__restrict__ packed,
                                                   float *__restrict__ scale,
-                                                  uint8_t *__restrict__ zero)
+                                                  uint8_t *__restrict__ zero, unsigned int *err)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(256) k_quantize(const float *__restrict__ w, i
             };
             const uint32_t two =
                 code(v.x) | (code(v.y) << 4) | (code(v.z) << 8) | (code(v.w) << 12);
-            reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = static_cast<uint16_t>(two);
-            if (lane == u) {
+            if (store_ok(gi * (G / 2) + 2 * lane, ngroups * (G / 2), err))
+                reinterpret_cast<uint16_t *>(packed + gi * (G / 2))[lane] = static_cast<uint16_t>(two);
+            if (lane == u && store_ok(gi, ngroups, err)) {
                 scale[gi] = mys;
                 zero[gi] = static_cast<uint8_t>(myz);
             }
@@ -206,7 +207,7 @@ __device__ __forceinline__ uint4 code_chunk(const uint8_t *__restrict__ packed, 
 // 69 sixteen-byte units per tile: 64 code chunks, 4 scale units, 1 zero unit.
 __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
                          const uint8_t *__restrict__ zero, int N, int K, int64_t ntiles_total,
-                         uint8_t *__restrict__ qw)
+                         uint8_t *__restrict__ qw, unsigned int *err)
 {
     const int NG = K / G;
     const int64_t units = ntiles_total * 69;
@@ -218,6 +219,7 @@ __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__rest
         const int g = static_cast<int>(tile % NG);
         const int64_t row0 = rt * TILE_ROWS;
         uint8_t *dst = qw + tile * TILE_BYTES;
+        if (!store_ok(tile * TILE_BYTES + unit * 16 + 15, ntiles_total * TILE_BYTES, err)) continue;
         if (unit < 64) {
             *reinterpret_cast<uint4 *>(dst + unit * 16) = code_chunk(packed, N, K, row0, g, unit);
         } else if (unit < 68) {
@@ -249,7 +251,7 @@ __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__rest
 // zero-nibble pairs and 8 bytes of padding.
 __global__ void k_repack_compact(const uint8_t *__restrict__ packed, const float *__restrict__ scale,
                                  const uint8_t *__restrict__ zero, int N, int K, int64_t ntiles_total,
-                                 uint8_t *__restrict__ qw)
+                                 uint8_t *__restrict__ qw, unsigned int *err)
 {
     const int NG = K / G;
     const int64_t units = ntiles_total * 67;
@@ -261,6 +263,8 @@ __global__ void k_repack_compact(const uint8_t *__restrict__ packed, const float
         const int g = static_cast<int>(tile % NG);
         const int64_t row0 = rt * TILE_ROWS;
         uint8_t *dst = qw + tile * CMP_TILE_BYTES;
+        if (!store_ok(tile * CMP_TILE_BYTES + unit * 16 + 15, ntiles_total * CMP_TILE_BYTES, err))
+            continue;
         if (unit < 64) {
             *reinterpret_cast<uint4 *>(dst + unit * 16) = code_chunk(packed, N, K, row0, g, unit);
         } else if (unit < 66) {
@@ -293,12 +297,13 @@ __global__ void k_repack_compact(const uint8_t *__restrict__ packed, const float
 // Code word i of chunk c of lane l of tile (row0, g) back into the
 // canonical bytes (rows past N are dropped).
 __device__ __forceinline__ void put_code_word(uint8_t *__restrict__ packed, int N, int K,
-                                              int64_t row0, int g, int c, int l, int i, uint32_t w)
+                                              int64_t row0, int g, int c, int l, int i, uint32_t w,
+                                              unsigned int *err)
 {
     const int r = l >> 2, t = l & 3, j = 4 * c + i;
     const int64_t kb = static_cast<int64_t>(g) * G + 16 * j + 2 * t;
     auto put = [&](int64_t row, int64_t k, int f) {
-        if (row < N) {
+        if (row < N && store_ok(row * (K / 2) + k / 2, static_cast<int64_t>(N) * (K / 2), err)) {
             const uint32_t lo = (w >> (4 * f)) & 15u, hi = (w >> (16 + 4 * f)) & 15u;
             packed[row * (K / 2) + k / 2] = static_cast<uint8_t>(lo | (hi << 4));
         }
@@ -313,7 +318,7 @@ __device__ __forceinline__ void put_code_word(uint8_t *__restrict__ packed, int 
 // row-pair for the metadata.
 __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t ntiles_total,
                          uint8_t *__restrict__ packed, float *__restrict__ scale,
-                         uint8_t *__restrict__ zero)
+                         uint8_t *__restrict__ zero, unsigned int *err)
 {
     const int NG = K / G;
     const int64_t units = ntiles_total * (256 + 8);
@@ -328,16 +333,17 @@ __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t n
         if (unit < 256) {
             const int c = unit >> 7, l = (unit >> 2) & 31, i = unit & 3;
             const uint32_t w = reinterpret_cast<const uint32_t *>(src)[(c * 32 + l) * 4 + i];
-            put_code_word(packed, N, K, row0, g, c, l, i, w);
+            put_code_word(packed, N, K, row0, g, c, l, i, w, err);
         } else {
             const int pair = unit - 256;
             const float *sp = reinterpret_cast<const float *>(src + SCALE_OFF) + 2 * pair;
             const uint8_t *zp = src + ZERO_OFF + 2 * pair;
-            if (row0 + pair < N) {
+            const int64_t lim = static_cast<int64_t>(N) * NG;
+            if (row0 + pair < N && store_ok((row0 + pair) * NG + g, lim, err)) {
                 scale[(row0 + pair) * NG + g] = sp[0];
                 zero[(row0 + pair) * NG + g] = zp[0];
             }
-            if (row0 + pair + 8 < N) {
+            if (row0 + pair + 8 < N && store_ok((row0 + pair + 8) * NG + g, lim, err)) {
                 scale[(row0 + pair + 8) * NG + g] = sp[1];
                 zero[(row0 + pair + 8) * NG + g] = zp[1];
             }
@@ -349,7 +355,7 @@ __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t n
 // per group.
 __global__ void k_unpack_compact(const uint8_t *__restrict__ qw, int N, int K, int64_t ntiles_total,
                                  uint8_t *__restrict__ packed, uint16_t *__restrict__ scale16,
-                                 uint8_t *__restrict__ zero)
+                                 uint8_t *__restrict__ zero, unsigned int *err)
 {
     const int NG = K / G;
     const int64_t units = ntiles_total * (256 + 8);
@@ -364,16 +370,17 @@ __global__ void k_unpack_compact(const uint8_t *__restrict__ qw, int N, int K, i
         if (unit < 256) {
             const int c = unit >> 7, l = (unit >> 2) & 31, i = unit & 3;
             const uint32_t w = reinterpret_cast<const uint32_t *>(src)[(c * 32 + l) * 4 + i];
-            put_code_word(packed, N, K, row0, g, c, l, i, w);
+            put_code_word(packed, N, K, row0, g, c, l, i, w, err);
         } else {
             const int pair = unit - 256;
             const uint16_t *sp = reinterpret_cast<const uint16_t *>(src + SCALE_OFF) + 2 * pair;
             const uint32_t zb = src[CMP_ZERO_OFF + pair];
-            if (row0 + pair < N) {
+            const int64_t lim = static_cast<int64_t>(N) * NG;
+            if (row0 + pair < N && store_ok((row0 + pair) * NG + g, lim, err)) {
                 scale16[(row0 + pair) * NG + g] = sp[0];
                 zero[(row0 + pair) * NG + g] = static_cast<uint8_t>(zb & 15u);
             }
-            if (row0 + pair + 8 < N) {
+            if (row0 + pair + 8 < N && store_ok((row0 + pair + 8) * NG + g, lim, err)) {
                 scale16[(row0 + pair + 8) * NG + g] = sp[1];
                 zero[(row0 + pair + 8) * NG + g] = static_cast<uint8_t>(zb >> 4);
             }
@@ -383,7 +390,7 @@ __global__ void k_unpack_compact(const uint8_t *__restrict__ qw, int N, int K, i
 
 // Activation group sums: one warp per (m, g), f32 accumulation.
 __global__ void k_xsum(const void *__restrict__ x, q4_dtype xt, int64_t M, int64_t K,
-                       float *__restrict__ xsum)
+                       float *__restrict__ xsum, unsigned int *err)
 {
     const int lane = threadIdx.x & 31;
     const int64_t NG = K / G, total = M * NG;
@@ -397,7 +404,7 @@ __global__ void k_xsum(const void *__restrict__ x, q4_dtype xt, int64_t M, int64
         for (int i = 0; i < 4; ++i) s += load_x_f32(x, xt, base + i);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) xsum[id] = s;
+        if (lane == 0 && store_ok(id, total, err)) xsum[id] = s;
     }
 }
 
@@ -410,59 +417,61 @@ static int grid_for(int64_t work, int threads)
 }
 
 cudaError_t quantize_launch(const float *w, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                            uint8_t *zero, bool symmetric, cudaStream_t s)
+                            uint8_t *zero, bool symmetric, unsigned int *err, cudaStream_t s)
 {
     const int64_t ngroups = N * K / G;
     const int grid = grid_for((ngroups + GPW - 1) / GPW * 32, 256);
     if (symmetric)
-        k_quantize<true><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero);
+        k_quantize<true><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero, err);
     else
-        k_quantize<false><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero);
+        k_quantize<false><<<grid, 256, 0, s>>>(w, ngroups, packed, scale, zero, err);
     return cudaGetLastError();
 }
 
 cudaError_t repack_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
-                          int64_t N, int64_t K, uint8_t *qw, cudaStream_t s)
+                          int64_t N, int64_t K, uint8_t *qw, unsigned int *err, cudaStream_t s)
 {
     const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
     k_repack<<<grid_for(ntiles * 69, 256), 256, 0, s>>>(packed, scale, zero, static_cast<int>(N),
-                                                        static_cast<int>(K), ntiles, qw);
+                                                        static_cast<int>(K), ntiles, qw, err);
     return cudaGetLastError();
 }
 
 cudaError_t unpack_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed, float *scale,
-                          uint8_t *zero, cudaStream_t s)
+                          uint8_t *zero, unsigned int *err, cudaStream_t s)
 {
     const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
     k_unpack<<<grid_for(ntiles * 264, 256), 256, 0, s>>>(qw, static_cast<int>(N),
                                                          static_cast<int>(K), ntiles, packed,
-                                                         scale, zero);
+                                                         scale, zero, err);
     return cudaGetLastError();
 }
 
 cudaError_t repack_compact_launch(const uint8_t *packed, const float *scale, const uint8_t *zero,
-                                  int64_t N, int64_t K, uint8_t *qw, cudaStream_t s)
+                                  int64_t N, int64_t K, uint8_t *qw, unsigned int *err,
+                                  cudaStream_t s)
 {
     const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
     k_repack_compact<<<grid_for(ntiles * 67, 256), 256, 0, s>>>(
-        packed, scale, zero, static_cast<int>(N), static_cast<int>(K), ntiles, qw);
+        packed, scale, zero, static_cast<int>(N), static_cast<int>(K), ntiles, qw, err);
     return cudaGetLastError();
 }
 
 cudaError_t unpack_compact_launch(const uint8_t *qw, int64_t N, int64_t K, uint8_t *packed,
-                                  uint16_t *scale16, uint8_t *zero, cudaStream_t s)
+                                  uint16_t *scale16, uint8_t *zero, unsigned int *err,
+                                  cudaStream_t s)
 {
     const int64_t ntiles = ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / G);
     k_unpack_compact<<<grid_for(ntiles * 264, 256), 256, 0, s>>>(
-        qw, static_cast<int>(N), static_cast<int>(K), ntiles, packed, scale16, zero);
+        qw, static_cast<int>(N), static_cast<int>(K), ntiles, packed, scale16, zero, err);
     return cudaGetLastError();
 }
 
 cudaError_t xsum_launch(const void *x, q4_dtype xt, int64_t M, int64_t K, float *xsum,
-                        cudaStream_t s)
+                        unsigned int *err, cudaStream_t s)
 {
     const int64_t total = M * (K / G);
-    k_xsum<<<grid_for(total * 32, 256), 256, 0, s>>>(x, xt, M, K, xsum);
+    k_xsum<<<grid_for(total * 32, 256), 256, 0, s>>>(x, xt, M, K, xsum, err);
     return cudaGetLastError();
 }
 
