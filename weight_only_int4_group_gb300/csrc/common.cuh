@@ -224,6 +224,20 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
     return d;
 }
 
+// d = a * 1 + c on a pair of 16-bit floats (bf16, or f16 when F16); exact
+// where it is used: a is offset + q, c = -(offset + zero), and the difference
+// q - zero is a small integer.
+template <bool F16>
+__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t c)
+{
+    uint32_t d;
+    if (F16)
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3C003C00u), "r"(c));
+    else
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(c));
+    return d;
+}
+
 // ------------------------------------------------------------ dtype helpers
 __device__ __forceinline__ float load_x_f32(const void *x, q4_dtype xt, int64_t i)
 {

@@ -208,19 +208,6 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[C])
         tmem_ld16x(taddr, v);
 }
 
-// d = a * 1 + c on a pair of 16-bit floats (bf16 or f16); exact here: a is
-// offset + q, c = -(offset + zero), the difference a small integer.
-template <bool F16>
-__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t c)
-{
-    uint32_t d;
-    if (F16)
-        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3C003C00u), "r"(c));
-    else
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(c));
-    return d;
-}
-
 struct Args {
     const uint8_t *qw;
     void *y;

@@ -59,8 +59,10 @@
 //     block needs no reduction across warps and a warp keeps 4x fewer
 //     accumulators; the step's activation rows (up to 16) are staged with
 //     the tiles and read as B fragments with ldmatrix (rows padded by 16
-//     bytes: conflict-free), the group sums come from one all-ones MMA per
-//     k-step and batch tile, shared by the warp's row tiles.
+//     bytes: conflict-free).  The A operand is the small integer q - zero
+//     itself (offset + q from the LOP3, minus offset + zero with one packed
+//     FMA, exact in bf16/f16), so no activation sums are needed: per group
+//     y += scale * D.  At 9..16 rows this saves a fifth of the MMAs.
 //
 // Both consumers read 1104-byte tiles (f32 scales, u8 zeros); the tensor-core
 // one also reads compact 1072-byte tiles (binary16 scales widened exactly,
@@ -293,9 +295,8 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
     constexpr int RB = RBT, TPW = RBT / W;
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     constexpr int TILES_BYTES = RBT * W * TBY;
-    const uint32_t MAG = ABT == 0 ? 0x43004300u : 0x64006400u;
-    const uint32_t ONES = ABT == 0 ? 0x3F803F80u : 0x3C003C00u;
-    const float OFF = ABT == 0 ? 128.0f : 1024.0f;
+    const uint32_t MAG = ABT == 0 ? 0x43004300u : 0x64006400u;  // offset + q: 128 + q or 1024 + q
+    const uint32_t NEG = ABT == 0 ? 0xC300C300u : 0xE400E400u;  // -(offset + zero), zero in the low bits
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, t = lane & 3;
     const int M = a.M;
@@ -347,12 +348,13 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
                     for (int jj = 0; jj < 4; ++jj)
                         ldmatrix_x4(bf[gp][n][2 * jj][0], bf[gp][n][2 * jj][1], bf[gp][n][2 * jj + 1][0],
                                     bf[gp][n][2 * jj + 1][1], xs + xoff[n] + (gi0 + gp) * G * 2 + jj * 64);
-            // this warp's row tiles of the groups: codes and metadata.  Tiles
-            // past the matrix (last row block) hold stale stage bytes; their
-            // rows are computed but never written out.
+            // this warp's row tiles of the groups: codes, scales and the
+            // packed -(offset + zero) of rows g and g + 8.  Tiles past the
+            // matrix (last row block) hold stale stage bytes; their rows are
+            // computed but never written out.
             uint32_t wv[GP][TPW][8];
             float2 sp[GP][TPW];
-            uint32_t zp[GP][TPW];
+            uint32_t nz[GP][TPW][2];
 #pragma unroll
             for (int gp = 0; gp < GP; ++gp)
 #pragma unroll
@@ -360,81 +362,58 @@ __device__ __forceinline__ void consume_rows(const GemvArgs &a, uint8_t *ring, i
                     const uint8_t *tile = stage + ((warp * TPW + r) * W + gi0 + gp) * TBY;
                     const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
                     const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + 512 + 16 * lane);
-                    tile_meta<CMP>(tile, gq, sp[gp][r], zp[gp][r]);
+                    uint32_t zp;
+                    tile_meta<CMP>(tile, gq, sp[gp][r], zp);
+                    nz[gp][r][0] = NEG | ((zp & 0xFFu) * 0x00010001u);
+                    nz[gp][r][1] = NEG | ((zp >> 8) * 0x00010001u);
                     wv[gp][r][0] = c0.x; wv[gp][r][1] = c0.y; wv[gp][r][2] = c0.z; wv[gp][r][3] = c0.w;
                     wv[gp][r][4] = c1.x; wv[gp][r][5] = c1.y; wv[gp][r][6] = c1.z; wv[gp][r][7] = c1.w;
                 }
             // k-step outer, groups and tiles inner: GP * TPW * NT independent
-            // accumulator chains plus the group sums.  One batch tile: an
-            // all-ones A times the activations gives lane (g, t) the sums of
-            // batch rows 2t, 2t + 1.  Two batch tiles: the 16 activation rows
-            // as A times all-ones B give lane (g, t) the sums of rows g and
-            // g + 8 (one MMA instead of two), redistributed by shuffles below.
-            float S[GP][NT][4], d[GP][TPW][NT][4];
+            // accumulator chains (a second chain per tile, even and odd
+            // k-steps apart, measured 1% slower).  The A operand is q - zero
+            // itself (offset + q from one LOP3, minus offset + zero by one
+            // packed FMA: exact), so the MMA yields sum (q - zero) x directly
+            // and a group costs one multiply by its scale.
+            float d[GP][TPW][NT][4];
 #pragma unroll
             for (int gp = 0; gp < GP; ++gp)
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int r = 0; r < TPW; ++r)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        S[gp][n][e] = 0.0f;
+                    for (int n = 0; n < NT; ++n)
 #pragma unroll
-                        for (int r = 0; r < TPW; ++r) d[gp][r][n][e] = 0.0f;
-                    }
+                        for (int e = 0; e < 4; ++e) d[gp][r][n][e] = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
 #pragma unroll
                 for (int gp = 0; gp < GP; ++gp) {
-                    if (NT == 1)
-                        mma_ab<ABT>(S[gp][0], ONES, ONES, ONES, ONES, bf[gp][0][j][0], bf[gp][0][j][1]);
-                    else
-                        mma_ab<ABT>(S[gp][0], bf[gp][0][j][0], bf[gp][NT - 1][j][0], bf[gp][0][j][1],
-                                    bf[gp][NT - 1][j][1], ONES, ONES);
 #pragma unroll
                     for (int r = 0; r < TPW; ++r) {
                         const uint32_t w = wv[gp][r][j];
-                        if (NT == 1) {
-                            mma_word<ABT>(d[gp][r][0], w, bf[gp][0][j][0], bf[gp][0][j][1]);
-                        } else {
-                            const uint32_t a0 = lop3_and_or(w, 0x000F000Fu, MAG);
-                            const uint32_t a1 = lop3_and_or(w >> 4, 0x000F000Fu, MAG);
-                            const uint32_t a3 = lop3_and_or(w >> 8, 0x000F000Fu, MAG);
-                            const uint32_t a2 = lop3_and_or(w >> 12, 0x000F000Fu, MAG);
+                        const uint32_t a0 = sub_pair<ABT != 0>(lop3_and_or(w, 0x000F000Fu, MAG), nz[gp][r][0]);
+                        const uint32_t a1 = sub_pair<ABT != 0>(lop3_and_or(w >> 4, 0x000F000Fu, MAG), nz[gp][r][1]);
+                        const uint32_t a3 = sub_pair<ABT != 0>(lop3_and_or(w >> 8, 0x000F000Fu, MAG), nz[gp][r][1]);
+                        const uint32_t a2 = sub_pair<ABT != 0>(lop3_and_or(w >> 12, 0x000F000Fu, MAG), nz[gp][r][0]);
 #pragma unroll
-                            for (int n = 0; n < NT; ++n)
-                                mma_ab<ABT>(d[gp][r][n], a0, a1, a2, a3, bf[gp][n][j][0], bf[gp][n][j][1]);
-                        }
+                        for (int n = 0; n < NT; ++n)
+                            mma_ab<ABT>(d[gp][r][n], a0, a1, a2, a3, bf[gp][n][j][0], bf[gp][n][j][1]);
                     }
                 }
             }
 #pragma unroll
             for (int gp = 0; gp < GP; ++gp) {
                 if (s * W + gi0 + gp >= NG) break;  // past K: nothing to add
-                float Sc[NT][2];  // sums of batch rows 8n + 2t and 8n + 2t + 1
-                if (NT == 1) {
-                    Sc[0][0] = S[gp][0][0];
-                    Sc[0][1] = S[gp][0][1];
-                } else {
-                    // S[gp][0][0] = sum of row g, S[gp][0][2] = sum of row g + 8
-                    Sc[0][0] = __shfl_sync(0xffffffffu, S[gp][0][0], 8 * t);
-                    Sc[0][1] = __shfl_sync(0xffffffffu, S[gp][0][0], 8 * t + 4);
-                    Sc[NT - 1][0] = __shfl_sync(0xffffffffu, S[gp][0][2], 8 * t);
-                    Sc[NT - 1][1] = __shfl_sync(0xffffffffu, S[gp][0][2], 8 * t + 4);
-                }
 #pragma unroll
-                for (int r = 0; r < TPW; ++r) {
-                    // OFF + zero: the byte under the exponent of 2^23
-                    const float zg = __uint_as_float(__byte_perm(zp[gp][r], 0x4B000000u, 0x7540)) - (8388608.0f - OFF);
-                    const float zg8 = __uint_as_float(__byte_perm(zp[gp][r], 0x4B000000u, 0x7541)) - (8388608.0f - OFF);
+                for (int r = 0; r < TPW; ++r)
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         float *ya = yacc[r][n];
-                        ya[0] = fmaf(sp[gp][r].x, fmaf(-zg, Sc[n][0], d[gp][r][n][0]), ya[0]);
-                        ya[1] = fmaf(sp[gp][r].x, fmaf(-zg, Sc[n][1], d[gp][r][n][1]), ya[1]);
-                        ya[2] = fmaf(sp[gp][r].y, fmaf(-zg8, Sc[n][0], d[gp][r][n][2]), ya[2]);
-                        ya[3] = fmaf(sp[gp][r].y, fmaf(-zg8, Sc[n][1], d[gp][r][n][3]), ya[3]);
+                        ya[0] = fmaf(sp[gp][r].x, d[gp][r][n][0], ya[0]);
+                        ya[1] = fmaf(sp[gp][r].x, d[gp][r][n][1], ya[1]);
+                        ya[2] = fmaf(sp[gp][r].y, d[gp][r][n][2], ya[2]);
+                        ya[3] = fmaf(sp[gp][r].y, d[gp][r][n][3], ya[3]);
                     }
-                }
             }
         }
         __syncwarp();
