@@ -641,21 +641,27 @@ def extra_rows(q4, torch, work, pk) -> dict:
     del g, xs, ys, ws8
 
     # Llama-7B-shaped layer, M = 1 (qkv 12288x4096, o 4096x4096, gate and up
-    # 11008x4096 each, down 4096x11008; 0.1% of input channels x20): 8
+    # 11008x4096 each, down 4096x11008; 0.1% of input channels x20): gate and
+    # up read the same activations and run as one 22016x4096 GEMV (their
+    # tiled buffers concatenated along the rows, as for the 70B step); 8
     # distinct layers per graph (0.87 GB, beyond L2), time per layer
-    shapes7 = [("qkv", 12288, 4096), ("o", 4096, 4096), ("gate", 11008, 4096), ("up", 11008, 4096),
+    mats7 = [("qkv", 12288, 4096), ("o", 4096, 4096), ("gate", 11008, 4096), ("up", 11008, 4096),
+             ("down", 4096, 11008)]
+    shapes7 = [("qkv", 12288, 4096), ("o", 4096, 4096), ("gate_up", 22016, 4096),
                ("down", 4096, 11008)]
     L7 = 8
     q7 = []
     for l in range(L7):
         mats = []
-        for i, (_, N, K) in enumerate(shapes7):
+        for i, (_, N, K) in enumerate(mats7):
             w = torch.empty((N, K), dtype=torch.float32, device=dev)
             cols = torch.from_numpy(synth.outlier_columns(70 + i, K).astype("int64")).to(dev)
             synth.dev_normal_f32(w.data_ptr(), N * K, 7000 + 10 * l + i, 0, SIGMA)
             w[:, cols] *= 20.0
             mats.append(q4.QWeight.from_float(w))
             del w
+        gate, up = mats[2], mats[3]
+        mats[2:4] = [q4.QWeight(torch.cat([gate.data, up.data]), gate.N + up.N, gate.K)]
         q7.append(mats)
     x7 = {}
     for _, N, K in shapes7:

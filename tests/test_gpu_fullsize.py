@@ -82,6 +82,38 @@ def test_7b_layer_with_outliers(N, K):
     _check_sampled(N, K, 1, seed=N + K, cols=cols)
 
 
+def test_7b_gate_up_rows_concatenated():
+    """Gate and up quantized separately and their tiled buffers concatenated
+    along the rows (11008 is a whole number of 16-row tiles): one 22016 x
+    4096 GEMV, as the 7B layer benchmark runs it; sampled rows of both halves
+    against the oracle, each half with its own outlier columns."""
+    import weight_only_int4_group_gb300 as q4
+    K, Nh = 4096, 11008
+    parts, meta = [], []
+    for h, seed in enumerate((301, 302)):
+        cols = synth.outlier_columns(210 + h, K)
+        w = _device_weights(Nh, K, seed, cols)
+        parts.append(q4.QWeight.from_float(w))
+        meta.append((seed, cols))
+        del w
+    fused = q4.QWeight(torch.cat([parts[0].data, parts[1].data]), 2 * Nh, K)
+    assert fused.nbytes == q4.weight_bytes(2 * Nh, K)
+    xbits = synth.normal_bf16(303, 0, K).reshape(1, K)
+    y = q4.gemv(dev_bf16_bits(xbits), fused, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert q4.check() == q4.OK
+    o = oracle.load()
+    xf = synth.bf16_bits_to_f32(xbits)
+    rng = np.random.default_rng(304)
+    for h, (seed, cols) in enumerate(meta):
+        for r in np.unique(np.concatenate([[0, Nh - 1], rng.integers(0, Nh, 12)])):
+            Wr = synth.normal_rows(seed, K, int(r), int(r) + 1, SIGMA, cols, 20.0)
+            pr, sr, zr = o.quantize(Wr)
+            yr, ar = o.dot_naive(xf, pr, sr, zr, 1, K)
+            col = h * Nh + int(r)
+            compare(y[:, col:col + 1], yr, ar, where=f"half {h} row {r}")
+
+
 def test_device_generator_matches_host():
     n = 1 << 16
     t = torch.empty(n, dtype=torch.float32, device="cuda")
