@@ -127,7 +127,17 @@ size_t q4_weight_bytes(int64_t N, int64_t K, q4_layout layout);
  * last tile are written as zeros.  qw must be 16-byte aligned and hold
  * q4_weight_bytes(N, K, Q4_LAYOUT_TILED) bytes; it may not overlap the
  * inputs.
- * Tile (row tile rt, group g) starts at byte (rt*(K/128) + g) * 1104:
+ * Tile order (both tiled layouts): blocks of 8 row tiles (128 rows); inside
+ * a block, steps of 4 groups (512 k); inside a step, row tile then group.
+ * With T = ceil(N/16) row tiles and NG = K/128 groups, tile (row tile rt,
+ * group g) is tile number
+ *     8*NG*b + nb*4*s + (rt - 8b)*ns + (g - 4s)
+ * where b = rt/8, s = g/4, nb = min(8, T - 8b) (row tiles in block b) and
+ * ns = min(4, NG - 4s) (groups in step s): one step of one block, which a
+ * decode GEMV reads as a unit, is one contiguous run of tiles.  Row-wise
+ * concatenation of two buffers is the buffer of the stacked matrix when the
+ * first has a multiple of 128 rows.
+ * Tile number t starts at byte t * 1104:
  *   bytes [0, 1024): 32 lanes x 2 chunks of 16 B; chunk c of lane l = 4 words,
  *     word i covers k-step j = 4c+i (k = 128g + 16j .. +15) for tile rows
  *     r = l/4 and r+8 and k offsets 2(l%4) + {0,1,8,9}; nibble fields (bit
@@ -150,8 +160,8 @@ q4_status q4_unpack(const void *qw, int64_t N, int64_t K, uint8_t *packed, float
  * fp16/bf16).  Same codes and zeros as the canonical arrays; each scale is
  * stored as IEEE binary16 rounded to nearest even (scales must lie in
  * binary16's normal range, 6.1e-5 .. 65504, to keep their precision), so
- * w_hat = (q - zero) * fp16(scale).  Tile (rt, g) at byte (rt*(K/128) + g) *
- * 1072: bytes [0, 1024) codes exactly as in the tiled layout above; [1024,
+ * w_hat = (q - zero) * fp16(scale).  Tiles in the order above, tile number
+ * t at byte t * 1072: bytes [0, 1024) codes exactly as in the tiled layout above; [1024,
  * 1056) binary16 scale pairs (s[i], s[i+8]) for i = 0..7; [1056, 1064) one
  * byte per pair, z[i] | z[i+8] << 4; [1064, 1072) zero padding (every tile
  * stays 16-byte aligned).  4.1875 bits per weight in memory.

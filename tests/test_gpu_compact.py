@@ -42,8 +42,14 @@ def test_repack_compact_bit_exact(N, K):
     assert np.array_equal(s16.cpu().numpy().view(np.uint16), so16)
     assert np.array_equal(z2.cpu().numpy(), zo)
     if N % 16:  # rows past N in the last tile are zero, padding included
-        t = qw.view((N + 15) // 16, K // 128, 1072)[-1].cpu().numpy()
-        sp = t[:, 1024:1056].view(np.uint16).reshape(K // 128, 8, 2)
+        # the last row tile's tiles, by the tile order include/q4.h states
+        T, NG = (N + 15) // 16, K // 128
+        b = (T - 1) // 8
+        nb = min(8, T - 8 * b)
+        tiles = qw.view(T * NG, 1072).cpu().numpy()
+        t = np.stack([tiles[8 * NG * b + nb * 4 * (g // 4) + (T - 1 - 8 * b) * min(4, NG - 4 * (g // 4))
+                            + g % 4] for g in range(NG)])
+        sp = t[:, 1024:1056].view(np.uint16).reshape(NG, 8, 2)
         for r in range(N % 16, 16):
             assert (sp[:, r % 8, r // 8] == 0).all()
         assert (t[:, 1064:] == 0).all()

@@ -122,9 +122,12 @@ def test_repack_unpack_round_trip(N, K):
     # padded rows of the last tile are zero
     ntiles = (N + 15) // 16
     if N % 16:
-        t = qw.view(ntiles, K // 128, 1104)[-1].cpu().numpy()
+        # the last row tile's tiles, found by the documented tile order
+        NG = K // 128
+        tiles = qw.view(ntiles * NG, 1104).cpu().numpy()
+        t = np.stack([tiles[_tile_number(ntiles - 1, g, ntiles, NG)] for g in range(NG)])
         # scale pairs of rows >= N (within the tile) are 0.0
-        sp = t[:, 1024:1088].view(np.float32).reshape(K // 128, 8, 2)
+        sp = t[:, 1024:1088].view(np.float32).reshape(NG, 8, 2)
         for r in range(N % 16, 16):
             assert (sp[:, r % 8, r // 8] == 0).all()
 
@@ -156,3 +159,41 @@ def test_xsum(dtype):
     got = q4.xsum(x).cpu().numpy().astype(np.float64)
     ref = oracle.load().xsum(xf)
     assert np.allclose(got, ref, rtol=1e-5, atol=1e-4)
+
+
+def _tile_number(rt, g, T, NG):
+    """The tile order include/q4.h states (restated independently here)."""
+    b, s = rt // 8, g // 4
+    nb, ns = min(8, T - 8 * b), min(4, NG - 4 * s)
+    return 8 * NG * b + nb * 4 * s + (rt - 8 * b) * ns + (g - 4 * s)
+
+
+@pytest.mark.parametrize("compact", [False, True])
+@pytest.mark.parametrize("N,K", [(300, 1152), (128, 512), (2000, 640)])
+def test_repack_tile_order(N, K, compact):
+    """Each tile's scales name its (row tile, group): every row of row tile
+    rt has scale 1 + rt + 128 g in group g (an integer below 2048, exact in
+    binary16), and every tile sits where the documented order puts it;
+    ragged last block (300 rows: 19 tiles) and last step (9 or 5 groups)."""
+    import weight_only_int4_group_gb300 as q4
+    T, NG = (N + 15) // 16, K // 128
+    packed = torch.zeros((N, K // 2), dtype=torch.uint8, device="cuda")
+    rows = torch.arange(N, dtype=torch.float32).view(N, 1)
+    groups = torch.arange(NG, dtype=torch.float32).view(1, NG)
+    scale = (rows // 16 + 128.0 * groups + 1.0).cuda()
+    zero = torch.zeros((N, NG), dtype=torch.uint8, device="cuda")
+    rep = q4.repack_compact if compact else q4.repack
+    tb = 1072 if compact else 1104
+    qw = rep(packed, scale, zero, N, K).cpu().numpy()
+    assert qw.size == T * NG * tb
+    seen = set()
+    for t in range(T * NG):
+        tile = qw[t * tb:(t + 1) * tb]
+        if compact:
+            s0 = float(tile[1024:1026].view(np.float16)[0])
+        else:
+            s0 = float(tile[1024:1028].view(np.float32)[0])
+        rt, g = int(s0 - 1) % 128, int(s0 - 1) // 128
+        assert _tile_number(rt, g, T, NG) == t, (t, rt, g)
+        seen.add((rt, g))
+    assert len(seen) == T * NG

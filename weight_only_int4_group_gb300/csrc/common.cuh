@@ -238,6 +238,44 @@ __device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t c)
     return d;
 }
 
+// ------------------------------------------------------------ tile order
+// Order of the tiles in both tiled layouts: blocks of LB_TILES row tiles
+// (128 rows); inside a block, steps of LB_GROUPS groups (512 k); inside a
+// step, row tile then group.  One step of one block -- the unit a decode
+// GEMV consumes -- is thus one contiguous run of up to 32 tiles.  The last
+// block may hold fewer row tiles and the last step fewer groups; every
+// earlier block and step is full.
+constexpr int LB_TILES = 8;
+constexpr int LB_GROUPS = 4;
+
+// Index (in tiles) of tile (row tile rt, group g) of a matrix of ntiles row
+// tiles and NG groups.
+__host__ __device__ __forceinline__ int64_t tile_index(int64_t rt, int g, int64_t ntiles, int NG)
+{
+    const int64_t rb = rt / LB_TILES;
+    const int64_t nrt = ntiles - rb * LB_TILES < LB_TILES ? ntiles - rb * LB_TILES : LB_TILES;
+    const int s = g / LB_GROUPS;
+    const int ng = NG - s * LB_GROUPS < LB_GROUPS ? NG - s * LB_GROUPS : LB_GROUPS;
+    return rb * LB_TILES * NG + s * nrt * LB_GROUPS + (rt - rb * LB_TILES) * ng + (g - s * LB_GROUPS);
+}
+
+// Inverse of tile_index: the (row tile, group) of the t-th tile.
+__host__ __device__ __forceinline__ void tile_of(int64_t t, int64_t ntiles, int NG, int64_t &rt, int &g)
+{
+    const int64_t per_block = static_cast<int64_t>(LB_TILES) * NG;
+    const int64_t rb = t / per_block;
+    const int64_t rem = t - rb * per_block;
+    const int64_t nrt = ntiles - rb * LB_TILES < LB_TILES ? ntiles - rb * LB_TILES : LB_TILES;
+    const int NS = (NG + LB_GROUPS - 1) / LB_GROUPS;
+    int64_t s = rem / (nrt * LB_GROUPS);
+    if (s > NS - 1) s = NS - 1;
+    const int64_t rem2 = rem - s * nrt * LB_GROUPS;
+    const int ng = NG - static_cast<int>(s) * LB_GROUPS < LB_GROUPS ? NG - static_cast<int>(s) * LB_GROUPS
+                                                                    : LB_GROUPS;
+    rt = rb * LB_TILES + rem2 / ng;
+    g = static_cast<int>(s) * LB_GROUPS + static_cast<int>(rem2 % ng);
+}
+
 // ------------------------------------------------------------ dtype helpers
 __device__ __forceinline__ float load_x_f32(const void *x, q4_dtype xt, int64_t i)
 {

@@ -69,6 +69,7 @@ namespace gm {
 
 constexpr int BN = 128;                    // weight rows per tile
 constexpr int RT = BN / TILE_ROWS;         // 8 packed tiles per group
+static_assert(RT == LB_TILES, "a tile's row tiles form one block of the weight layout");
 constexpr int C_STAGE = RT * TILE_BYTES;   // 8832 bytes of codes per group (compact: 8576 used)
 constexpr int THREADS = 608;
 constexpr uint32_t TMEM_COLS = 512;
@@ -398,10 +399,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&cfull[c], static_cast<uint32_t>(nrt) * TBY);
+                    // the tile's 8 row tiles lie in one block of the weight
+                    // layout: group g of each, ng tiles apart
+                    const int64_t t0 = tile_index(rt0, g, ntiles_rows, NG);
+                    const int ng = min(LB_GROUPS, NG - (g / LB_GROUPS) * LB_GROUPS);
                     for (int r = 0; r < nrt; ++r)
-                        bulk_g2s(sC + c * C_STAGE + r * TBY,
-                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g) * TBY, TBY,
-                                 &cfull[c]);
+                        bulk_g2s(sC + c * C_STAGE + r * TBY, a.qw + (t0 + r * ng) * TBY, TBY, &cfull[c]);
                     ++i;
                 }
             }

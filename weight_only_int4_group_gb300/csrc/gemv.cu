@@ -91,6 +91,10 @@ constexpr int WARP_PAIR_FLOATS = 4 * PAIR_STRIDE + 4 * 4;
 constexpr int MIN_BLOCKS = 2;  // CTAs per SM the shared memory budget is sized for
 
 constexpr int XROW = W * G * 2 + 16;  // MMA staged activations: one padded row per batch row
+// a step is one step of the weight layout's blocks, and a row block lies in
+// one layout block: the tiles of an item are one contiguous run
+static_assert(W == LB_GROUPS && LB_TILES % RB == 0 && LB_TILES % RB_SMALL_ROWS == 0,
+              "row blocks and steps nest in the weight layout's blocks");
 
 // xrows: batch rows staged with each step (MMA, M <= 8); 0 otherwise;
 // tb: bytes per tile (TILE_BYTES, or CMP_TILE_BYTES for compact metadata)
@@ -543,10 +547,15 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) k_gemv(const GemvArgs a)
                                             : static_cast<uint32_t>(xrows) * ng * G * 2;
                     uint8_t *stage = ring + slot * SB;
                     mbar_arrive_expect_tx(&full[slot], row_bytes * nrt + xbytes);
-                    for (int r = 0; r < nrt; ++r)
-                        bulk_g2s(stage + r * W * TBY,
-                                 a.qw + (static_cast<int64_t>(rt0 + r) * NG + g0) * TBY,
-                                 row_bytes, &full[slot]);
+                    // the step's tiles are contiguous in the weight buffer,
+                    // row tile by row tile: one copy for a full step, one
+                    // per row tile (to the stage's 4-group stride) otherwise
+                    const uint8_t *src = a.qw + tile_index(rt0, g0, ntiles, NG) * TBY;
+                    if (ng == W)
+                        bulk_g2s(stage, src, row_bytes * nrt, &full[slot]);
+                    else
+                        for (int r = 0; r < nrt; ++r)
+                            bulk_g2s(stage + r * W * TBY, src + r * row_bytes, row_bytes, &full[slot]);
                     if (gstep < npro) {
                         pro_g0[gstep] = g0;
                         pro_ng[gstep] = ng;

@@ -215,8 +215,9 @@ __global__ void k_repack(const uint8_t *__restrict__ packed, const float *__rest
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t tile = u / 69;
         const int unit = static_cast<int>(u % 69);
-        const int64_t rt = tile / NG;
-        const int g = static_cast<int>(tile % NG);
+        int64_t rt;
+        int g;
+        tile_of(tile, (N + TILE_ROWS - 1) / TILE_ROWS, NG, rt, g);
         const int64_t row0 = rt * TILE_ROWS;
         uint8_t *dst = qw + tile * TILE_BYTES;
         if (!store_ok(tile * TILE_BYTES + unit * 16 + 15, ntiles_total * TILE_BYTES, err)) continue;
@@ -259,8 +260,9 @@ __global__ void k_repack_compact(const uint8_t *__restrict__ packed, const float
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t tile = u / 67;
         const int unit = static_cast<int>(u % 67);
-        const int64_t rt = tile / NG;
-        const int g = static_cast<int>(tile % NG);
+        int64_t rt;
+        int g;
+        tile_of(tile, (N + TILE_ROWS - 1) / TILE_ROWS, NG, rt, g);
         const int64_t row0 = rt * TILE_ROWS;
         uint8_t *dst = qw + tile * CMP_TILE_BYTES;
         if (!store_ok(tile * CMP_TILE_BYTES + unit * 16 + 15, ntiles_total * CMP_TILE_BYTES, err))
@@ -326,8 +328,9 @@ __global__ void k_unpack(const uint8_t *__restrict__ qw, int N, int K, int64_t n
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t tile = u / 264;
         const int unit = static_cast<int>(u % 264);
-        const int64_t rt = tile / NG;
-        const int g = static_cast<int>(tile % NG);
+        int64_t rt;
+        int g;
+        tile_of(tile, (N + TILE_ROWS - 1) / TILE_ROWS, NG, rt, g);
         const int64_t row0 = rt * TILE_ROWS;
         const uint8_t *src = qw + tile * TILE_BYTES;
         if (unit < 256) {
@@ -363,8 +366,9 @@ __global__ void k_unpack_compact(const uint8_t *__restrict__ qw, int N, int K, i
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t tile = u / 264;
         const int unit = static_cast<int>(u % 264);
-        const int64_t rt = tile / NG;
-        const int g = static_cast<int>(tile % NG);
+        int64_t rt;
+        int g;
+        tile_of(tile, (N + TILE_ROWS - 1) / TILE_ROWS, NG, rt, g);
         const int64_t row0 = rt * TILE_ROWS;
         const uint8_t *src = qw + tile * CMP_TILE_BYTES;
         if (unit < 256) {
