@@ -14,13 +14,17 @@
 // (page "LLM Quantization Architecture in Depth", "Kernels and memory
 // layout").
 //
-// One persistent CTA per SM, 19 warps with fixed roles (a warp reaches the
-// tensor-memory lanes of quadrant warp % 4 only):
+// One persistent CTA per SM, 20 warps with fixed roles (a warp reaches the
+// tensor-memory lanes of quadrant warp % 4 only, and runs on SM partition
+// warp % 4):
 //   warp 0      activation producer: X tiles by 2-D tensor TMA (128-byte
 //               swizzle, K-major), one stage per group;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma;
-//   warp 2      weight producer: the group's 8 packed tiles (16 rows each)
-//               by 1-D bulk copies into a ring of code stages;
+//   warp 19     weight producer: the group's 8 packed tiles (16 rows each)
+//               by 1-D bulk copies into a ring of code stages (on partition
+//               3, which has no other producer: the builders of the
+//               partition that also runs a producer fall behind the others,
+//               and the MMAs wait for the slowest builder; warp 2 idles);
 //   warps 3-10  operand builders, two per tensor-memory lane quadrant (one
 //               per half of the group's k): each thread owns one weight row,
 //               turns its 64 codes into 32 packed (q - zero) pairs with a
@@ -71,7 +75,15 @@ constexpr int BN = 128;                    // weight rows per tile
 constexpr int RT = BN / TILE_ROWS;         // 8 packed tiles per group
 static_assert(RT == LB_TILES, "a tile's row tiles form one block of the weight layout");
 constexpr int C_STAGE = RT * TILE_BYTES;   // 8832 bytes of codes per group (compact: 8576 used)
-constexpr int THREADS = 608;
+#ifndef GEMM_WPROD
+#define GEMM_WPROD 19
+#endif
+// The weight producer has a warp of its own on SM partition 3, the one
+// partition without a producer or the MMA thread (a warp reaches the
+// tensor-memory lanes of its partition only, so every partition already
+// runs two operand builders and two rescale warps); warp 2 idles.
+constexpr int WPROD = GEMM_WPROD;
+constexpr int THREADS = (WPROD == 19 ? 20 : 19) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL = 256;            // first tensor-memory column of the A stages
 constexpr int NS = 4;                      // activation / A stages
@@ -381,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = max(0, i - NS); j < i; ++j)
                 mbar_wait_bounded(&xfull[j % NS], (j / NS) & 1, abort_flag, a.wait_ns, a.err, false);
         }
-    } else if (warp == 2) {
+    } else if (warp == WPROD) {
         // ----------------------------------------------------- weight producer
         if (lane == 0 && !a.debug_no_copy) {
             Cursor cur = cur0;
@@ -430,24 +442,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xs = smem_u32(sX + s * X_ST);
+                    // one descriptor per stage; a k step's operand lies a
+                    // constant number of 16-byte units further on
+                    const uint64_t xd = sw128_desc(smem_u32(sX + s * X_ST));
                     const uint32_t at = tmem + A_COL + static_cast<uint32_t>(s) * 64u;
                     if constexpr (BT <= 64) {
                         // two accumulators (k halves 0-63 and 64-127), interleaved
                         const uint32_t d0 = tmem + static_cast<uint32_t>(b) * 128u;
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            mma_ts(d0, at + 8u * k, sw128_desc(xs + 32 * k), idesc, k > 0 ? 1u : 0u);
-                            mma_ts(d0 + 64u, at + 32u + 8u * k, sw128_desc(xs + X_HALF + 32 * k),
-                                   idesc, k > 0 ? 1u : 0u);
+                            mma_ts(d0, at + 8u * k, xd + (32 * k) / 16, idesc, k > 0 ? 1u : 0u);
+                            mma_ts(d0 + 64u, at + 32u + 8u * k, xd + (X_HALF + 32 * k) / 16, idesc,
+                                   k > 0 ? 1u : 0u);
                         }
                     } else {
                         const uint32_t d = tmem + static_cast<uint32_t>(b) * 128u;
 #pragma unroll
                         for (int k16 = 0; k16 < 8; ++k16)
-                            mma_ts(d, at + 8u * k16,
-                                   sw128_desc(xs + (k16 >> 2) * X_HALF + 32 * (k16 & 3)), idesc,
-                                   k16 > 0 ? 1u : 0u);
+                            mma_ts(d, at + 8u * k16, xd + ((k16 >> 2) * X_HALF + 32 * (k16 & 3)) / 16,
+                                   idesc, k16 > 0 ? 1u : 0u);
                     }
                     issued = true;
                     mma_commit(&mdone[s]);
@@ -561,7 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ++i;
             }
         }
-    } else if (warp >= 11) {
+    } else if (warp >= 11 && warp < 19) {
         // ------------------------------------------------ rescale + epilogue
         const int w = warp - 11, q = warp & 3, ch = w >> 2;
         const int R = 32 * q + lane;
