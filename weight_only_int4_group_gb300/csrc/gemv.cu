@@ -1259,12 +1259,14 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     cudaGetDevice(&dev);
     cudaError_t cfg = dispatch(cmp, path, M, xt, false, false,
                                [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
-    // Fewer than 4 steps per CTA with 8-tile row blocks, 2 <= M <= 16: use
-    // 4-tile ones (one row tile per consumer warp), so that steps are short
-    // and plentiful (at M = 1 the longer steps win).
+    // Few steps per CTA with 8-tile row blocks, 2 <= M <= 16: use 4-tile
+    // ones (one row tile per consumer warp), so that steps are short and
+    // plentiful -- below 4 steps per CTA up to 4 rows, below 8 beyond (the
+    // 70B decode step measured: 8 at M <= 4 cost 4% at M = 2, and gained
+    // 1-2.5% at M = 8 and 16; at M = 1 the longer steps win).
     const int64_t T8 = static_cast<int64_t>((ntiles + RB - 1) / RB) * NS;
-    p.small = T8 < 4 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 2 &&
-              xt != Q4_F32;
+    p.small = T8 < (M > 4 ? 8 : 4) * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA &&
+              M >= 2 && xt != Q4_F32;
     if (p.small && cfg == cudaSuccess)
         cfg = dispatch(cmp, path, M, xt, false, true,
                        [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
