@@ -7,10 +7,10 @@
 // turned into floating point in registers and never written back to memory.
 //
 // Work decomposition (stream-K): the output rows are cut into row blocks of
-// RB = 8 tiles (128 rows; 2 tiles when 2 <= M <= 8 and 8-tile blocks would
-// give each CTA fewer than 4 steps); each row block is a sequence of
-// NS = ceil(NG/4)
-// steps, a step being 4 consecutive groups along K.  The nrb * NS items are
+// RB = 8 tiles (128 rows; 4 tiles when 9 <= M <= 16 and 8-tile blocks would
+// give each CTA fewer than 8 steps); each row block is a sequence of
+// NS = ceil(NG/4) steps, a step being 4 consecutive groups along K (one
+// contiguous run of the weight layout's tiles).  The nrb * NS items are
 // split into `grid` contiguous, equal ranges, one per persistent CTA (two
 // CTAs per SM).  A CTA accumulates the steps of a row block in registers and
 // writes the row block out when it reaches its last step; a row block whose
@@ -54,7 +54,7 @@
 //     activations come from one extra MMA per k-step with an all-ones A
 //     operand.  Per group, y += scale * (D - (offset + zero) * sum x).
 //
-//   Row-split MMA (2 <= M <= 16, bf16/f16 activations): consumer warp w
+//   Row-split MMA (9 <= M <= 16, bf16/f16 activations): consumer warp w
 //     takes row tiles w * RB/4 .. of every step, all 4 groups, so a row
 //     block needs no reduction across warps and a warp keeps 4x fewer
 //     accumulators; the step's activation rows (up to 16) are staged with
@@ -62,7 +62,9 @@
 //     bytes: conflict-free).  The A operand is the small integer q - zero
 //     itself (offset + q from the LOP3, minus offset + zero with one packed
 //     FMA, exact in bf16/f16), so no activation sums are needed: per group
-//     y += scale * D.  At 9..16 rows this saves a fifth of the MMAs.
+//     y += scale * D, a fifth fewer MMAs than with activation sums.  For
+//     2 <= M <= 8 the group-split MMA consumer above is faster (measured
+//     3-11% per launch and 1-10% on the 70B decode step).
 //
 // Both consumers read 1104-byte tiles (f32 scales, u8 zeros); the tensor-core
 // one also reads compact 1072-byte tiles (binary16 scales widened exactly,
@@ -1153,22 +1155,21 @@ static cudaError_t dispatch_t(int path, int M, q4_dtype xt, bool deep, bool smal
         if constexpr (CMP) return cudaErrorInvalidValue;  // rejected before planning
         else return f(Kern<PATH_FMA, 1, 0, false>{});
     }
-    // 2 <= M <= 16, 16-bit activations: row-split consumers (4-tile row
-    // blocks for small problems)
-    if (M >= 2 && xt != Q4_F32) {
-        const bool two = M > 8;
+    // 2 <= M <= 8, 16-bit activations: group-split consumers, one MMA
+    // column tile for the batch rows, the step's activation rows staged
+    if (M >= 2 && M <= 8 && xt != Q4_F32) {
+        if (xt == Q4_F16) return f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB, CMP>{});
+        return f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB, CMP>{});
+    }
+    // 9 <= M <= 16, 16-bit activations: row-split consumers, two MMA column
+    // tiles (4-tile row blocks for small problems)
+    if (M >= 9 && xt != Q4_F32) {
         if (small) {
-            if (xt == Q4_F16)
-                return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{})
-                           : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
-            return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{})
-                       : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
+            if (xt == Q4_F16) return f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
+            return f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB_SMALL_ROWS, CMP, true>{});
         }
-        if (xt == Q4_F16)
-            return two ? f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB, CMP, true>{})
-                       : f(Kern<PATH_MMA, 1, 1, false, NSTAGE, false, RB, CMP, true>{});
-        return two ? f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB, CMP, true>{})
-                   : f(Kern<PATH_MMA, 1, 0, false, NSTAGE, false, RB, CMP, true>{});
+        if (xt == Q4_F16) return f(Kern<PATH_MMA, 2, 1, false, NSTAGE, false, RB, CMP, true>{});
+        return f(Kern<PATH_MMA, 2, 0, false, NSTAGE, false, RB, CMP, true>{});
     }
     // deep: M = 1, where a 3-stage ring still fits two CTAs per SM
     const bool two = M > 8;
@@ -1259,14 +1260,14 @@ static GemvPlan make_plan(int M, int N, int K, q4_dtype xt, int path, int sm_cou
     cudaGetDevice(&dev);
     cudaError_t cfg = dispatch(cmp, path, M, xt, false, false,
                                [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
-    // Few steps per CTA with 8-tile row blocks, 2 <= M <= 16: use 4-tile
-    // ones (one row tile per consumer warp), so that steps are short and
-    // plentiful -- below 4 steps per CTA up to 4 rows, below 8 beyond (the
-    // 70B decode step measured: 8 at M <= 4 cost 4% at M = 2, and gained
-    // 1-2.5% at M = 8 and 16; at M = 1 the longer steps win).
+    // Fewer than 8 steps per CTA with 8-tile row blocks, 9 <= M <= 16 (the
+    // row-split consumers): use 4-tile ones (one row tile per consumer
+    // warp), so that steps are short and plentiful (the 70B decode step at
+    // M = 16: 2.4% faster than below 4 steps; the group-split consumers of
+    // M <= 8 keep 8-tile blocks).
     const int64_t T8 = static_cast<int64_t>((ntiles + RB - 1) / RB) * NS;
-    p.small = T8 < (M > 4 ? 8 : 4) * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA &&
-              M >= 2 && xt != Q4_F32;
+    p.small = T8 < 8 * static_cast<int64_t>(sm_count) * per_sm && path == PATH_MMA && M >= 9 &&
+              xt != Q4_F32;
     if (p.small && cfg == cudaSuccess)
         cfg = dispatch(cmp, path, M, xt, false, true,
                        [&](auto k) { return decltype(k)::configure(dev, M, &per_sm); });
