@@ -240,7 +240,8 @@ def test_debug_bounds_selftest():
 PARITY_UNDER_DEBUG = ["tests/test_gpu_canaries.py", "tests/test_gpu_quantize.py",
                       "tests/test_gpu_quantize_sym.py", "tests/test_gpu_compact.py",
                       "tests/test_gpu_gemv.py", "tests/test_gpu_gemm.py",
-                      "tests/test_gpu_fullsize.py", "tests/test_zz_no_alloc.py"]
+                      "tests/test_gpu_fullsize.py", "tests/test_gpu_random_shapes.py",
+                      "tests/test_zz_no_alloc.py"]
 
 
 @pytest.mark.skipif(UNDER_DEBUG, reason="already running against the debug library")
@@ -258,5 +259,5 @@ def test_parity_suites_under_debug_build():
     assert r.returncode == 0, tail
     passed = re.search(r"(\d+) passed", r.stdout)
     assert passed and "failed" not in r.stdout, tail
-    # every collected test ran (the suites hold about two hundred)
-    assert int(passed.group(1)) >= 150, tail
+    # every collected test ran (the suites hold about four hundred)
+    assert int(passed.group(1)) >= 300, tail
