@@ -35,7 +35,10 @@ def test_gemm_small_k_many_rows(K, dist):
     averaged away: 4096 rows x 256 tokens, three seeds, plain N(0, 0.02)
     weights and weights with one input channel scaled x20 (most weights of
     that group then quantize to the zero point).  f32 output, so the
-    comparison sees the product itself."""
+    comparison sees the product itself.  Each weight enters the tensor cores
+    rounded once to binary16 (relative error at most 2^-11), so no element
+    may use more than 2^-11 / 1e-3 = 0.49 of the tolerance, whatever the
+    signs line up to."""
     import weight_only_int4_group_gb300 as q4
     N, M = 4096, 256
     worst = 0.0
@@ -49,8 +52,8 @@ def test_gemm_small_k_many_rows(K, dist):
         assert q4.check() == q4.OK
         worst = max(worst, compare(y, y_ref, absdot, where=f"K={K} {dist} seed {seed}")
                     ["max_err_over_tol"])
-    # no rounding of the weights: the error is f32 accumulation noise
-    assert worst < 0.05, worst
+    # the worst case of one binary16 rounding per term, plus f32 accumulation
+    assert worst < 2.0 ** -11 / 1e-3 + 0.01, worst
 
 
 @pytest.mark.parametrize("M", [1, 9, 16, 17, 32, 48, 64, 100, 128, 129, 255])
