@@ -731,7 +731,11 @@ def extra_rows(q4, torch, work, pk) -> dict:
             q4.gemm(xg, qq, out=yg, ws=wsg)
         g = graph_of(torch, grun)
         t = time_graph(torch, g, reps=10)
-        rows[rname] = {"shape": f"M={Mg} N={Ng} K={Kg} bf16", "ms": round(t * 1e3, 3),
+        rows[rname] = {"shape": f"M={Mg} N={Ng} K={Kg} bf16",
+                       "operands": "binary16 weights (one rounding) and activations (exact) behind "
+                                   "power-of-two row/token scalings, f32 accumulation; prep, GEMM "
+                                   "and scratch-clear passes all timed",
+                       "ms": round(t * 1e3, 3),
                        "TFLOP/s": round(flops / t / 1e12, 1),
                        "frac_of_bf16_peak": round(flops / t / 1e12 / pk["bf16_tflops"], 4),
                        "peak": pk["bf16_tflops"], "peak_kind": "burst, of measured"}

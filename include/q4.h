@@ -257,31 +257,39 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
  * Large-M W4A16 GEMM, Y[M][N] = X[M][K] * W_hat[N][K]^T (prefill; page
  * "LLM Quantization Architecture in Depth", section "Kernels and memory
  * layout": the kernel loads packed codes and scales, dequantizes on chip and
- * feeds the tensor cores in the same pass).  Computed group by group as the
- * page "Weight quantization" factors it ("How it works": one multiply per
- * group): the tcgen05 tensor cores form D_g[n][m] = sum_{k in g} (q - zero)
- * * x[m][k] from the exact small integers q - zero (in the activations'
- * 16-bit type) with f32 accumulation in tensor memory, and each group's D_g
- * is scaled by scale[n][g] and added up in f32.  No weight is rounded to
- * 16 bits, so the result differs from the exact product only by f32
- * rounding.
+ * feeds the tensor cores in the same pass).  Both tensor-core operands are
+ * binary16 behind exact powers of two: each weight row is scaled by 2^-e[n]
+ * (15 * its largest group scale lands in [2^14, 2^15)) and each weight
+ * w_hat = scale * (q - zero) is rounded once to binary16 (relative error at
+ * most 2^-11); each token row is scaled by 2^-a[m] (its largest |x| lands
+ * in the same range) and converted exactly.  The tcgen05 tensor cores
+ * accumulate in f32 and the result is scaled back by 2^(e[n] + a[m]).  So
+ * |Y - exact| <= 2^-11 * sum |w_hat x| + f32 accumulation, within the page's
+ * 1e-3 * sum |w_hat x| at any K.  (A group whose scale is more than 2^20
+ * below its row's largest, or a token row whose |x| spans more than about
+ * 2^31, loses the excess precision to binary16's subnormal range.)
+ * One call runs three passes on `stream`: the normalizations and, for bf16
+ * activations, the binary16 copy of x into the workspace; the GEMM kernel;
+ * the scratch part of the workspace set back to zero.
  * x: [M][K] BF16 or F16 (16-byte aligned); qw: as for q4_gemv; y: [M][N]
  * BF16, F16 or F32.  Any M >= 1 and N >= 1.  Each CTA tile covers 128
  * weight rows and the smallest of 16, 32, 64 or 128 tokens that covers M
  * (128 beyond); when the tiles are too few to fill the GPU, the groups of a
  * tile are split over several CTAs and their f32 partial sums added in a
- * fixed order through the workspace (q4_gemm_workspace_bytes; the
- * workspace rule of q4_gemv_workspace_bytes applies).  Errors as q4_gemv
- * (UNSUPPORTED for F32 activations).
+ * fixed order through the workspace.  Workspace: q4_gemm_workspace_bytes
+ * (always needed; the workspace rule of q4_gemv_workspace_bytes applies).
+ * Errors as q4_gemv (UNSUPPORTED for F32 activations).
  */
 q4_status q4_gemm(const void *x, q4_dtype xt, int64_t M, int64_t N, int64_t K, const void *qw,
                   q4_layout layout, size_t qw_bytes, void *y, q4_dtype yt, void *workspace,
                   size_t workspace_bytes, q4_stream_t stream);
 
-/* Workspace bytes q4_gemm needs for this problem on the current device (0
- * when every tile is computed by one CTA): one u32 arrival counter per
- * tile, padded to 256 B, then f32 partial sums.  Same rule as
- * q4_gemv_workspace_bytes. */
+/* Workspace bytes q4_gemm needs for this problem on the current device:
+ * one u32 arrival counter per tile, padded to 256 B, and f32 partial sums
+ * (only when tiles are split over CTAs), then the scratch of the first pass
+ * (row and token factors, f32; the binary16 copy of x, 2 * M * K bytes),
+ * each part 1024-byte aligned.  Same rule as q4_gemv_workspace_bytes: a
+ * completed call leaves all of it zero. */
 size_t q4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Diagnostic for the GEMM's bounded waits: launches q4_gemm's kernel with

@@ -1,4 +1,4 @@
-"""W4A16 GEMM (tcgen05, exact per group) through the C ABI against the
+"""W4A16 GEMM (tcgen05, binary16 operands) through the C ABI against the
 oracle's plain dequantize-then-dot, element by element, under the stated
 tolerance."""
 import numpy as np

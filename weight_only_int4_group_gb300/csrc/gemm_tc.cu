@@ -20,7 +20,10 @@
 // 2^-11 * sum |w_hat x| (about 0.49e-3) plus f32 accumulation, inside the
 // 1e-3 * sum |w_hat x| bound at any K and any sign pattern.  RN16(s * t)
 // comes from the scale split into binary16 halves, s = hi + lo, as
-// fma(hi, t, lo * t) on packed pairs (t = q - zero exact in binary16).
+// fma(hi, t, lo * t) on packed pairs (t = q - zero exact in binary16).  The
+// bound holds for groups within 2^20 of their row's largest scale and token
+// rows whose |x| spans less than about 2^31; beyond that binary16's
+// subnormal range takes the excess precision.
 //
 // Passes of one call (one stream, in order):
 //   1. k_prep: per weight row 2^-e[n] from its scales; per token row 2^a[m]
@@ -35,14 +38,21 @@
 //   warp 0      activation producer: x' tiles by 2-D tensor TMA (128-byte
 //               swizzle, K-major), one stage per group;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma;
-//   warp 3      weight producer: the group's 8 packed tiles (16 rows each)
-//               by 1-D bulk copies into a ring of code stages;
-//   warps 4-19  operand builders, four per tensor-memory lane quadrant (one
-//               per quarter of the group's k): each thread owns one weight
-//               row and turns its 32 codes into 16 packed w' pairs (shift,
-//               LOP3, one packed subtraction for q - zero, one packed multiply
-//               and one packed FMA), stored with tcgen05.st as the MMA's A
-//               operand in tensor memory;
+//   warp 3      weight producer: one 1-D bulk copy per step of the weight
+//               layout (the tile's 8 row tiles x 4 groups, one contiguous
+//               run of packed tiles) into a ring of code stages -- one copy
+//               per group was measured to leave this thread, issuing eight,
+//               the slowest link of the pipeline;
+//   warps 4-19  operand builders in teams that take groups in turn: two
+//               teams of 8 warps with 128-token tiles (a warp = one k half of
+//               one lane quadrant), four teams of 4 with fewer tokens (a warp
+//               = one quadrant's whole group).  Each thread owns one weight
+//               row and turns its codes into packed w' pairs (shift, LOP3, one
+//               packed subtraction for q - zero, one packed multiply and one
+//               packed FMA per pair), stored with tcgen05.st as the MMA's A
+//               operand in tensor memory.  One team alone could not keep up:
+//               a group's build is a chain of waits, loads, unpacking and a
+//               tensor-memory store;
 //   warps 20-23 epilogue, one per quadrant: at the end of a tile each thread
 //               loads its row's accumulator (tcgen05.ld), scales it by
 //               2^(e[n] + a[m]) and stores it (or a partial sum, below);
