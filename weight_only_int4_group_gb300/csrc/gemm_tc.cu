@@ -370,28 +370,32 @@ __device__ __forceinline__ int norm_exp(uint32_t ebits, bool zero)
 }
 __device__ __forceinline__ float pow2f(int p) { return __uint_as_float(static_cast<uint32_t>(127 + p) << 23); }
 
-// Warps [0, row_warps) take one 16-row weight tile each: the largest scale
-// of each row over all its groups gives rowinv[n] = 2^-e[n], e[n] from
-// 15 * max scale (the largest |q - zero| is 15).  The remaining warps take
-// one token row each: 2^a[m] from the row's largest |x| goes to tokf[m]
-// and, for bf16 activations (xp not null), x * 2^-a[m] to xp as binary16
-// (exact: a bf16 value keeps its 8 significant bits).  f16 activations get
-// a[m] = 0 and are not copied.
+// Blocks [0, row_blocks) take one 16-row weight tile per warp: the largest
+// scale of each row over all its groups gives rowinv[n] = 2^-e[n], e[n] from
+// 15 * max scale (the largest |q - zero| is 15).  Each later block takes one
+// token row: 2^a[m] from the row's largest |x| goes to tokf[m] and, for bf16
+// activations (xp not null), x * 2^-a[m] to xp as binary16 (exact: a bf16
+// value keeps its 8 significant bits).  f16 activations get a[m] = 0 and are
+// not copied.  A whole block per token row keeps many loads in flight when
+// there are few tokens.
+constexpr int PREP_THREADS = 256;
 template <bool CMP>
-__global__ void __launch_bounds__(256) k_prep(const uint8_t *qw, int N, int K, float *rowinv,
-                                              int row_warps, const __nv_bfloat16 *x, int M,
-                                              __half *xp, float *tokf, unsigned int *err)
+__global__ void __launch_bounds__(PREP_THREADS) k_prep(const uint8_t *qw, int N, int K, float *rowinv,
+                                                       int row_blocks, const __nv_bfloat16 *x, int M,
+                                                       __half *xp, float *tokf, unsigned int *err)
 {
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
-    const int wid = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    if (wid < row_warps) {
+    if (static_cast<int>(blockIdx.x) < row_blocks) {
+        const int wid = static_cast<int>(blockIdx.x) * (PREP_THREADS / 32) + (threadIdx.x >> 5);
         const int NG = K / G;
         const int64_t ntiles = (N + TILE_ROWS - 1) / TILE_ROWS;
+        if (wid >= ntiles) return;
         // scale j of a tile belongs to row (j >> 1) + 8 (j & 1)
         uint32_t mx[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) mx[j] = 0u;
+#pragma unroll 2
         for (int g = lane; g < NG; g += 32) {
             const uint8_t *t = qw + tile_index(wid, g, ntiles, NG) * TBY + SCALE_OFF;
             if (CMP) {
@@ -430,27 +434,34 @@ __global__ void __launch_bounds__(256) k_prep(const uint8_t *qw, int N, int K, f
         }
         return;
     }
-    const int m = wid - row_warps;
+    const int m = static_cast<int>(blockIdx.x) - row_blocks;
     if (m >= M) return;
     if (!xp) {  // f16 activations: used as they are
-        if (lane == 0 && store_ok(m, M, err)) tokf[m] = 1.0f;
+        if (threadIdx.x == 0 && store_ok(m, M, err)) tokf[m] = 1.0f;
         return;
     }
     const uint4 *row = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(m) * K);
     uint4 *out = reinterpret_cast<uint4 *>(xp + static_cast<int64_t>(m) * K);
     const int nv = K / 8;
     uint32_t amax = 0u;  // bf16 magnitude bits; their order is the order of |x|
-    for (int v = lane; v < nv; v += 32) {
+#pragma unroll 4
+    for (int v = threadIdx.x; v < nv; v += PREP_THREADS) {
         const uint4 w = row[v];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) amax = max(amax, max(ws[j] & 0x7FFFu, (ws[j] >> 16) & 0x7FFFu));
     }
+    __shared__ uint32_t red[PREP_THREADS / 32];
     amax = __reduce_max_sync(0xffffffffu, amax);
+    if (lane == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < PREP_THREADS / 32; ++w) amax = max(amax, red[w]);
     const int am = norm_exp(min((amax >> 7) & 0xFFu, 254u), amax == 0u);
     const float inv = pow2f(-am);
-    if (lane == 0 && store_ok(m, M, err)) tokf[m] = pow2f(am);
-    for (int v = lane; v < nv; v += 32) {
+    if (threadIdx.x == 0 && store_ok(m, M, err)) tokf[m] = pow2f(am);
+#pragma unroll 4
+    for (int v = threadIdx.x; v < nv; v += PREP_THREADS) {
         const uint4 w = row[v];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
@@ -1006,18 +1017,18 @@ q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int
     __half *xp = reinterpret_cast<__half *>(ws + sl.xp);
 
     // pass 1: row and token normalizations, the binary16 copy of bf16 activations
-    const int row_warps = static_cast<int>((N + TILE_ROWS - 1) / TILE_ROWS);
-    const int64_t warps = row_warps + M;
-    const int prep_blocks = static_cast<int>((warps + 7) / 8);
+    const int64_t row_tiles = (N + TILE_ROWS - 1) / TILE_ROWS;
+    const int row_blocks = static_cast<int>((row_tiles + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32));
+    const int prep_blocks = static_cast<int>(row_blocks + M);
     const auto *xb = static_cast<const __nv_bfloat16 *>(f16 ? nullptr : x);
     if (cmp)
-        k_prep<true><<<prep_blocks, 256, 0, s>>>(qw, static_cast<int>(N), static_cast<int>(K), rowinv,
-                                                 row_warps, xb, static_cast<int>(M), f16 ? nullptr : xp,
-                                                 tokf, err);
+        k_prep<true><<<prep_blocks, PREP_THREADS, 0, s>>>(qw, static_cast<int>(N), static_cast<int>(K),
+                                                          rowinv, row_blocks, xb, static_cast<int>(M),
+                                                          f16 ? nullptr : xp, tokf, err);
     else
-        k_prep<false><<<prep_blocks, 256, 0, s>>>(qw, static_cast<int>(N), static_cast<int>(K), rowinv,
-                                                  row_warps, xb, static_cast<int>(M), f16 ? nullptr : xp,
-                                                  tokf, err);
+        k_prep<false><<<prep_blocks, PREP_THREADS, 0, s>>>(qw, static_cast<int>(N), static_cast<int>(K),
+                                                           rowinv, row_blocks, xb, static_cast<int>(M),
+                                                           f16 ? nullptr : xp, tokf, err);
     *cerr = cudaGetLastError();
     if (*cerr != cudaSuccess) return Q4_ERR_CUDA;
 
