@@ -274,7 +274,8 @@ q4_status q4_gemv_timeout_selftest(const void *x, q4_dtype xt, int64_t M, int64_
  * x: [M][K] BF16 or F16 (16-byte aligned); qw: as for q4_gemv; y: [M][N]
  * BF16, F16 or F32.  Any M >= 1 and N >= 1.  Each CTA tile covers 128
  * weight rows and the smallest of 16, 32, 64 or 128 tokens that covers M
- * (128 beyond); when the tiles are too few to fill the GPU, the groups of a
+ * (128 beyond, or 256 when 256-token tiles alone give every SM eight or
+ * more); when the tiles are too few to fill the GPU, the groups of a
  * tile are split over several CTAs and their f32 partial sums added in a
  * fixed order through the workspace.  Workspace: q4_gemm_workspace_bytes
  * (always needed; the workspace rule of q4_gemv_workspace_bytes applies).

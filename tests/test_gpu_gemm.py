@@ -214,3 +214,31 @@ def test_gemm_prefill_shape_sampled():
         p, s, z = o.quantize(Wr)
         yr, ar = o.dot_naive(xf, p, s, z, 1, K)
         compare(y[torch.from_numpy(ms).cuda(), int(r):int(r) + 1], yr, ar, where=f"row {r}")
+
+
+@pytest.mark.parametrize("xdt,compact", [(torch.bfloat16, False), (torch.float16, True)])
+def test_gemm_256_token_tiles(xdt, compact):
+    """A shape whose 256-token tiles alone give every SM of a 152-SM GPU
+    eight or more (3 token tiles x 407 row blocks = 1221), so the GEMM takes
+    256-token tiles with one tensor-memory accumulator per tile: ragged in
+    both M (513 = 2 x 256 + 1) and N, every element against the oracle."""
+    import weight_only_int4_group_gb300 as q4
+    M, N, K = 513, 407 * 128 - 5, 128
+    W = synth.normal_rows(77, K, 0, N, 0.02)
+    x, xf = x_for(xdt, M, K, seed=78)
+    o = oracle.load()
+    p, s, z = o.quantize(W)
+    dev = [torch.from_numpy(a).cuda() for a in (p, s, z)]
+    if compact:
+        qw = q4.QWeight(q4.repack_compact(*dev, N, K), N, K, True)
+        s16, z4 = o.compact_meta(s, z)
+        s, z = o.expand_meta(s16, z4, K // 128)
+    else:
+        qw = q4.QWeight(q4.repack(*dev, N, K), N, K)
+    ws = q4.gemm_workspace(M, N, K)
+    y = q4.gemm(x, qw, out_dtype=torch.bfloat16, ws=ws)
+    torch.cuda.synchronize()
+    assert q4.check() == q4.OK
+    assert int(ws.count_nonzero()) == 0
+    y_ref, absdot = o.dot_naive(xf, p, s, z, N, K, threads=16)
+    compare(y, y_ref, absdot, where=f"256-token tiles {xdt} compact={compact}")

@@ -59,13 +59,16 @@
 //   warp 2      idle.
 // Tensor memory (512 columns): the tile accumulator double-buffered in
 // columns [0, 256) (one tile accumulates while the epilogue drains the
-// other), four A stages of one group each at 256 + 64 s.  With at most 64
+// other; a 256-token tile's single accumulator fills them, and the epilogue
+// drains it before the next tile starts), four A stages of one group each at
+// 256 + 64 s.  With at most 64
 // tokens the MMAs of each group alternate between two accumulators (its two k
 // halves, summed by the epilogue): an MMA of fewer than 128 columns takes
 // about 51 cycles however small, so a single dependent chain would leave the
 // tensor core idle.
 // A CTA tile is 128 weight rows x BT tokens, BT the smallest of 16, 32, 64,
-// 128 that covers M (128 beyond): 128 x BT x 16 MMAs, A from tensor memory,
+// 128 that covers M (128 beyond; 256 when 256-token tiles alone give every
+// CTA many whole tiles): 128 x BT x 16 MMAs, A from tensor memory,
 // B = the activation rows from shared memory.  Per group the MMA thread waits
 // for "A built and activations landed" (one builder of the team waits for the
 // latter before it arrives), issues the group's 8 MMAs in one block and
@@ -105,7 +108,7 @@ constexpr int W_B0 = 4, NBLD = 16;          // builders: warps 4..19
 constexpr int W_E0 = 20, NEPI = 4;          // epilogue: warps 20..23
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL = 256;            // first tensor-memory column of the A stages
-constexpr int NS = 4;                      // activation / A stages
+constexpr int NS = 4;                      // A stages (tensor memory)
 constexpr int BAND = 8;                    // token tiles per raster band
 // Normalizing exponents are kept in [-EMAX, EMAX]: 2^-e and 2^e stay normal
 // f32 numbers.
@@ -122,14 +125,21 @@ struct Plan {
     static constexpr int TEAM = NBLD / TEAMS;
     static constexpr int X_HALF = BT * 64 * 2;    // one 64-k half of a group's activations
     static constexpr int X_ST = 2 * X_HALF;
+    // 256-token tiles: two activation stages (64 KB each) and one tile
+    // accumulator (256 columns; the A stages take the rest of tensor
+    // memory), so the epilogue drains it before the next tile starts
+    static constexpr int NSX = BT >= 256 ? 2 : NS;  // activation stages
+    static constexpr int NDB = BT >= 256 ? 1 : 2;   // tile accumulators
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_C = NS * X_ST;
+    static constexpr int OFF_C = NSX * X_ST;
     static constexpr int OFF_BAR = ((OFF_C + NC * C_STAGE + 15) / 16) * 16;
-    static constexpr int NBAR = 3 * NS + 2 * NC + 5;
+    static constexpr int NBAR = NSX + 2 * NS + 2 * NC + 5;
     static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
     static_assert(X_HALF % 1024 == 0, "swizzled halves start on 1024-byte boundaries");
     static_assert(NS % TEAMS == 0, "each builder team keeps its own A stages");
+    static_assert(NSX % TEAMS == 0 && NSX <= NS, "activation stages follow the A stages");
+    static_assert(A_COL >= static_cast<uint32_t>(NDB * (BT > 128 ? BT : 128)), "accumulators fit below the A stages");
     static_assert(TEAM % 4 == 0, "a team covers the four lane quadrants");
     static_assert(SMEM_ALLOC <= 227 * 1024, "one CTA per SM");
 };
@@ -485,7 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmx, const Args a)
 {
     using P = Plan<BT>;
-    constexpr int NC = P::NC, X_HALF = P::X_HALF, X_ST = P::X_ST;
+    constexpr int NC = P::NC, X_HALF = P::X_HALF, X_ST = P::X_ST, NSX = P::NSX, NDB = P::NDB;
     constexpr int TEAMS = P::TEAMS, TEAM = P::TEAM;
     constexpr int TBY = CMP ? CMP_TILE_BYTES : TILE_BYTES;
     constexpr bool TWO = BT <= 64;               // two accumulators (a group's k halves)
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // stages (a step of up to 4 groups; every builder warp releases each);
     // dfull: a tile's accumulator complete; dempty: read by the epilogue.
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
-    uint64_t *xfull = bar, *afull = xfull + NS, *mdone = afull + NS;
+    uint64_t *xfull = bar, *afull = xfull + NSX, *mdone = afull + NS;
     uint64_t *cfull = mdone + NS, *cempty = cfull + NC;
     uint64_t *dfull = cempty + NC, *dempty = dfull + 2, *drain = dempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -523,8 +533,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < NSX; ++i) mbar_init(&xfull[i], 1);
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&xfull[i], 1);
             mbar_init(&afull[i], TEAM);
             mbar_init(&mdone[i], 1);
         }
@@ -556,22 +566,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int mb, nb;
                 tile_coords(tile, a.mt, a.nt, mb, nb);
                 for (int g = g0; g < g1; ++g) {
-                    const int s = i % NS;
-                    if (i >= NS && !mbar_wait_bounded(&mdone[s], ((i / NS) - 1) & 1, abort_flag,
-                                                      a.wait_ns, a.err)) {
+                    // stage x is free once the MMAs of group i - NSX completed
+                    const int x = i % NSX, r = i - NSX;
+                    if (r >= 0 && !mbar_wait_bounded(&mdone[r % NS], (r / NS) & 1, abort_flag,
+                                                     a.wait_ns, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&xfull[s], static_cast<uint32_t>(X_ST));
-                    uint8_t *dst = sX + s * X_ST;
-                    tma_load_2d(dst, &tmx, g * G, mb * BT, &xfull[s]);
-                    tma_load_2d(dst + X_HALF, &tmx, g * G + 64, mb * BT, &xfull[s]);
+                    mbar_arrive_expect_tx(&xfull[x], static_cast<uint32_t>(X_ST));
+                    uint8_t *dst = sX + x * X_ST;
+                    tma_load_2d(dst, &tmx, g * G, mb * BT, &xfull[x]);
+                    tma_load_2d(dst + X_HALF, &tmx, g * G + 64, mb * BT, &xfull[x]);
                     ++i;
                 }
             }
             // every issued copy lands before the CTA may exit
-            for (int j = max(0, i - NS); j < i; ++j)
-                mbar_wait_bounded(&xfull[j % NS], (j / NS) & 1, abort_flag, a.wait_ns, a.err, false);
+            for (int j = max(0, i - NSX); j < i; ++j)
+                mbar_wait_bounded(&xfull[j % NSX], (j / NSX) & 1, abort_flag, a.wait_ns, a.err, false);
         }
     } else if (warp == W_W) {
         // ----------------------------------------------------- weight producer
@@ -611,10 +622,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             int tile, g0, g1, i = 0, u = 0;
             bool ok = true, issued = false;
             while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
-                const int b = u & 1;
+                const int b = u % NDB;
                 // the epilogue has read this accumulator's previous tile
-                if (u >= 2 && !mbar_wait_bounded(&dempty[b], ((u >> 1) - 1) & 1, abort_flag,
-                                                 a.wait_ns, a.err, true, true)) {
+                if (u >= NDB && !mbar_wait_bounded(&dempty[b], ((u / NDB) - 1) & 1, abort_flag,
+                                                   a.wait_ns, a.err, true, true)) {
                     ok = false;
                     break;
                 }
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     // one descriptor per stage; a k step's operand lies a
                     // constant number of 16-byte units further on
-                    const uint64_t xd = sw128_desc(smem_u32(sX + s * X_ST));
+                    const uint64_t xd = sw128_desc(smem_u32(sX + (i % NSX) * X_ST));
                     const uint32_t at = tmem + A_COL + static_cast<uint32_t>(s) * 64u;
                     const uint32_t acc = g > g0 ? 1u : 0u;  // the tile's first k step starts the sum
                     uint32_t dd[8], aa[8];
@@ -762,7 +773,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // group i read is in place
                 bool landed = true;
                 if (wt == 0)
-                    landed = mbar_wait_bounded(&xfull[s], (i / NS) & 1, abort_flag, a.wait_ns, a.err);
+                    landed = mbar_wait_bounded(&xfull[i % NSX], (i / NSX) & 1, abort_flag, a.wait_ns,
+                                               a.err);
                 __syncwarp();
                 if (!__all_sync(0xffffffffu, landed)) {
                     ok = false;
@@ -783,12 +795,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         int tile, g0, g1, u = 0;
         bool ok = true;
         while (ok && next_unit(a, NG, cur, tile, g0, g1)) {
-            const int b = u & 1;
+            const int b = u % NDB;
             int mb, nb;
             tile_coords(tile, a.mt, a.nt, mb, nb);
             const int n = nb * BN + R;
             const float fn = n < a.N ? __frcp_rn(a.rowinv[n]) : 0.0f;  // 2^e[n], exact
-            ok = mbar_wait_bounded(&dfull[b], (u >> 1) & 1, abort_flag, a.wait_ns, a.err);
+            ok = mbar_wait_bounded(&dfull[b], (u / NDB) & 1, abort_flag, a.wait_ns, a.err);
             ok = __all_sync(0xffffffffu, ok);
             const int64_t first = static_cast<int64_t>(tile) * NG;
             int c_first = blockIdx.x, nc = 1;
@@ -935,11 +947,12 @@ static KernFn kernel_for(int bt, int *smem)
     case 16: *smem = Plan<16>::SMEM_ALLOC; return k_gemm<16, CMP>;
     case 32: *smem = Plan<32>::SMEM_ALLOC; return k_gemm<32, CMP>;
     case 64: *smem = Plan<64>::SMEM_ALLOC; return k_gemm<64, CMP>;
-    default: *smem = Plan<128>::SMEM_ALLOC; return k_gemm<128, CMP>;
+    case 128: *smem = Plan<128>::SMEM_ALLOC; return k_gemm<128, CMP>;
+    default: *smem = Plan<256>::SMEM_ALLOC; return k_gemm<256, CMP>;
     }
 }
 
-static int bt_index(int bt) { return bt == 16 ? 0 : bt == 32 ? 1 : bt == 64 ? 2 : 3; }
+static int bt_index(int bt) { return bt == 16 ? 0 : bt == 32 ? 1 : bt == 64 ? 2 : bt == 128 ? 3 : 4; }
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -977,8 +990,12 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count)
     GemmPlan p{};
     p.bt = 16;
     while (p.bt < 128 && p.bt < M) p.bt *= 2;
-    p.mt = static_cast<int>((M + p.bt - 1) / p.bt);
     p.nt = static_cast<int>((N + BN - 1) / BN);
+    // 256-token tiles (twice the MMA work per group built) only when they
+    // alone give every CTA many whole tiles: split over CTAs, their single
+    // accumulator stalls at every short unit (measured 35% slower there)
+    if (M > 128 && ((M + 255) / 256) * p.nt >= 8LL * sm_count) p.bt = 256;
+    p.mt = static_cast<int>((M + p.bt - 1) / p.bt);
     const int64_t T = static_cast<int64_t>(p.mt) * p.nt;
     const int64_t NG = K / G;
     // Whole tiles in turn when every CTA gets many (the last round costs at
@@ -1063,8 +1080,8 @@ q4_status gemm_run(const GemmPlan &p, const void *x, q4_dtype xt, int64_t M, int
     a.debug_no_copy = debug_no_copy;
     int smem = 0;
     const KernFn kern = cmp ? kernel_for<true>(p.bt, &smem) : kernel_for<false>(p.bt, &smem);
-    const int variant = (cmp ? 4 : 0) + bt_index(p.bt);
-    static std::atomic<bool> configured[8][64];  // concurrent first calls may both set it
+    const int variant = (cmp ? 5 : 0) + bt_index(p.bt);
+    static std::atomic<bool> configured[10][64];  // concurrent first calls may both set it
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[variant][dev].load(std::memory_order_relaxed)) {
