@@ -44,9 +44,9 @@
 //               per group was measured to leave this thread, issuing eight,
 //               the slowest link of the pipeline;
 //   warps 4-19  operand builders in teams that take groups in turn: two
-//               teams of 8 warps with 128-token tiles (a warp = one k half of
-//               one lane quadrant), four teams of 4 with fewer tokens (a warp
-//               = one quadrant's whole group).  Each thread owns one weight
+//               teams of 8 warps with 128- and 256-token tiles (a warp = one
+//               k half of one lane quadrant), four teams of 4 with fewer
+//               tokens (a warp = one quadrant's whole group).  Each thread owns one weight
 //               row and turns its codes into packed w' pairs (shift, LOP3, one
 //               packed subtraction for q - zero, one packed multiply and one
 //               packed FMA per pair), stored with tcgen05.st as the MMA's A
@@ -61,11 +61,10 @@
 // columns [0, 256) (one tile accumulates while the epilogue drains the
 // other; a 256-token tile's single accumulator fills them, and the epilogue
 // drains it before the next tile starts), four A stages of one group each at
-// 256 + 64 s.  With at most 64
-// tokens the MMAs of each group alternate between two accumulators (its two k
-// halves, summed by the epilogue): an MMA of fewer than 128 columns takes
-// about 51 cycles however small, so a single dependent chain would leave the
-// tensor core idle.
+// 256 + 64 s.  With at most 64 tokens the MMAs of each group alternate
+// between two accumulators (its two k halves, summed by the epilogue): an MMA
+// of fewer than 128 columns takes about 51 cycles however small, so a single
+// dependent chain would leave the tensor core idle.
 // A CTA tile is 128 weight rows x BT tokens, BT the smallest of 16, 32, 64,
 // 128 that covers M (128 beyond; 256 when 256-token tiles alone give every
 // CTA many whole tiles): 128 x BT x 16 MMAs, A from tensor memory,
@@ -118,9 +117,8 @@ template <int BT>
 struct Plan {
     static constexpr int NC = BT >= 128 ? 2 : 4;  // code stages (steps of 4 groups)
     // Builder teams take groups in turn: two teams of 8 warps (one k half of
-    // one lane quadrant each) with 128-token tiles, four teams of 4 warps
-    // (a whole group of one quadrant each) with fewer tokens, where the MMAs
-    // are short and the builders alone set the pace.
+    // one lane quadrant each) with 128- and 256-token tiles, four teams of 4
+    // warps (a whole group of one quadrant each) with fewer tokens.
     static constexpr int TEAMS = BT >= 128 ? 2 : 4;
     static constexpr int TEAM = NBLD / TEAMS;
     static constexpr int X_HALF = BT * 64 * 2;    // one 64-k half of a group's activations
